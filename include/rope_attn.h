@@ -1,0 +1,159 @@
+/*
+ * rope_attn.h -- C ABI of librope_attn.so: rotary position embedding (RoPE)
+ * and causal attention with RoPE fused in, for NVIDIA GB300 (sm_103a).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Pointers named *device* must point to memory the current CUDA device can
+ *   read/write (cudaMalloc, PyTorch CUDA tensors).  Pointers named *host*
+ *   are ordinary host memory.  The caller owns every buffer; no entry point
+ *   allocates or frees memory.
+ * - Work is enqueued on the stream `s` (0 = legacy default stream) of the
+ *   current device and runs asynchronously; entry points return as soon as
+ *   the kernels are launched.
+ * - Errors are returned as ra_status codes, never thrown.  Every argument
+ *   check happens on the host before any CUDA call, so a rejected call has
+ *   no side effect.  ra_last_error() gives a readable reason.
+ * - Errors found by a kernel while it runs (a position outside the table)
+ *   are recorded in a per-device status word that ra_get_device_status()
+ *   reads and clears.
+ * - Element strides are counted in elements, not bytes; the innermost
+ *   (head-dimension) stride is always 1.
+ *
+ * Sources (page title, section) for what each call computes:
+ *  [RF] "RoPE and FlashAttention: relative positions and online softmax":
+ *       1 (pair rotation, theta_i = base^(-2i/d)), 2 (absolute positions,
+ *       decoder cache convention), 4 (S = QK^T/sqrt(d), P = softmax(S),
+ *       O = PV), 5 (online softmax with running max / denominator /
+ *       numerator; offset-causal mask j <= off + i).
+ *  [TR] "Write Triton Rope Kernel": layouts (NeoX halves vs GPT-J pairs),
+ *       fp32 cos/sin tables [max_seq_len, D/2], per-token positions[],
+ *       partial rot_dim, H_q != H_kv, in-place vs out-of-place, one launch
+ *       for Q and K.
+ *  [PM] "RoPE + PoPE Attention Kernels" (pope-memory-optimal README): rotate
+ *       inside the attention kernel instead of materialising rotated Q/K.
+ */
+#ifndef ROPE_ATTN_H
+#define ROPE_ATTN_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  RA_OK = 0,
+  RA_ERR_INVALID_ARG = -1,     /* a size, pointer or parameter is out of range        */
+  RA_ERR_UNSUPPORTED = -2,     /* valid, but this build has no kernel for the case   */
+  RA_ERR_ALIGNMENT = -3,       /* pointer or stride misaligned for the requested path */
+  RA_ERR_OVERLAP = -4,         /* an output partially overlaps an input               */
+  RA_ERR_CUDA = -5,            /* a CUDA runtime call failed (see ra_last_error)      */
+  RA_ERR_DEVICE_TIMEOUT = -6,  /* a kernel gave up waiting on an internal barrier     */
+  RA_ERR_POSITION_RANGE = -7   /* a kernel met a position outside [0, table_rows)     */
+} ra_status;
+
+typedef enum { RA_NEOX = 0, RA_GPTJ = 1 } ra_layout;
+typedef enum { RA_F32 = 0, RA_BF16 = 1, RA_F16 = 2 } ra_dtype;
+
+/*
+ * rope_tables_build -- fill the fp32 cos/sin tables.
+ *   Defines: theta_i = base^(-2i/F), i in [0, rot_dim/2), F = freq_dim, or
+ *   rot_dim when freq_dim <= 0 ([RF] 1; [TR] Correctness requirements);
+ *   cos_out[p][i] = cos(p * theta_i), sin_out[p][i] = sin(p * theta_i) for
+ *   p in [0, rows).  The angle and both functions are evaluated in fp64 and
+ *   rounded once to fp32 ([TR]: tables built in fp32 or better; [RF] 2:
+ *   keep the angle policy explicit at long positions).
+ *   cos_out, sin_out: device, each [rows][rot_dim/2] fp32, row stride
+ *     rot_dim/2 elements, written entirely.
+ *   rows >= 0, rot_dim even and >= 2, base > 0.
+ */
+ra_status rope_tables_build(float *cos_out, float *sin_out, int64_t rows, int rot_dim,
+                            double base, int freq_dim, cudaStream_t s);
+
+/*
+ * rope_apply_qk -- rotate Q and K of a packed token batch in one launch
+ * ([TR] Required reasoning process, Kernel design rules; [RF] 2).
+ *   Token t of every head is rotated at position positions[t] (never the
+ *   token index).  Only the first rot_dim dims of each head are rotated:
+ *     layout RA_NEOX: pairs (i, i + rot_dim/2);  RA_GPTJ: pairs (2i, 2i+1);
+ *     lo' = lo*cos - hi*sin,  hi' = hi*cos + lo*sin,  i < rot_dim/2,
+ *   with cos/sin read from table row positions[t] (row stride rot_dim/2).
+ *   Arithmetic is fp32; results are rounded to dt (round to nearest even).
+ *   Dims [rot_dim, D) are left untouched in place and copied out of place.
+ *   V is never passed here.
+ *   q: device [T][Hq][D] of dt, element strides strides_q = {token, head}.
+ *   k: device [T][Hkv][D] of dt, strides strides_k.  q may be NULL iff
+ *     Hq == 0, k may be NULL iff Hkv == 0.
+ *   q_out, k_out: NULL or equal to q / k for in place (strides ignored);
+ *     otherwise distinct device buffers with strides strides_qo / strides_ko
+ *     that must not overlap any input or the other output (RA_ERR_OVERLAP).
+ *   positions: device [T], int32 (pos_is_int64 = 0) or int64.
+ *   cos_t, sin_t: device tables from rope_tables_build with the same
+ *     rot_dim and table_rows rows.  A position outside [0, table_rows)
+ *     leaves that token's outputs unwritten and records
+ *     RA_ERR_POSITION_RANGE in the device status word.
+ *   T >= 0 (T == 0: nothing launched), D even, 2 <= rot_dim <= D, rot_dim
+ *   even.  Aligned vector access is used when every pointer is 16-byte
+ *   aligned and every stride and offset is a multiple of 16 bytes; other
+ *   cases take a scalar kernel.
+ */
+ra_status rope_apply_qk(void *q, void *k, void *q_out, void *k_out, ra_dtype dt, int64_t T,
+                        int Hq, int Hkv, int D, int rot_dim, ra_layout layout,
+                        const int64_t strides_q[2], const int64_t strides_k[2],
+                        const int64_t strides_qo[2], const int64_t strides_ko[2],
+                        const void *positions, int pos_is_int64, const float *cos_t,
+                        const float *sin_t, int64_t table_rows, cudaStream_t s);
+
+/*
+ * attn_fwd_causal_rope -- causal softmax attention forward with RoPE applied
+ * to Q and K inside the kernel ([PM]; [RF] 1, 4, 5).
+ *   Query row i of (b, h) sits at absolute position kv_offset + i; key row j
+ *   sits at position j.  With apply_rope != 0 both are rotated as in
+ *   rope_apply_qk (same layout, rot_dim, tables) before the product; no
+ *   rotated tensor is written to memory.  V is never rotated.
+ *     s_ij = softmax_scale * <q~_i, k~_j>  for j <= kv_offset + i and j < Sk,
+ *     O_i  = sum_j exp(s_ij - m_i) V_j / l_i,  l_i = sum_j exp(s_ij - m_i),
+ *     LSE_i = m_i + ln(l_i)  (natural log, scale included).
+ *   q-head h reads kv-head h / (Hq / Hkv) (grouped-query attention).
+ *   q: device [B][Hq][Sq][D], strides strides_q = {b, h, s};
+ *   k, v: device [B][Hkv][Sk][D], strides strides_k / strides_v;
+ *   o: device [B][Hq][Sq][D] of dt, strides strides_o;
+ *   lse: device fp32 [B][Hq][Sq] contiguous, or NULL (not written).
+ *   dt RA_F32 runs an fp32 CUDA-core kernel (D <= 256).  RA_BF16 / RA_F16 run
+ *   the tensor-core kernel (tcgen05): D in {64, 128}; every pointer 16-byte
+ *   aligned and every stride a multiple of 8 elements; rotated Q/K enter the
+ *   product as fp16, P and V as dt, accumulation fp32.
+ *   kv_offset >= 0 (so every row sees key 0; a negative offset would leave
+ *   rows without keys and is rejected), Sk >= 1, Sq >= 0 (0: no launch).
+ *   With apply_rope: 2 <= rot_dim <= D, even, and table_rows >=
+ *   max(Sk, kv_offset + Sq).  softmax_scale <= 0 selects 1/sqrt(D).
+ */
+ra_status attn_fwd_causal_rope(const void *q, const void *k, const void *v, void *o, float *lse,
+                               ra_dtype dt, int B, int Hq, int Hkv, int64_t Sq, int64_t Sk,
+                               int D, int64_t kv_offset, int apply_rope, int rot_dim,
+                               ra_layout layout, const float *cos_t, const float *sin_t,
+                               int64_t table_rows, float softmax_scale,
+                               const int64_t strides_q[3], const int64_t strides_k[3],
+                               const int64_t strides_v[3], const int64_t strides_o[3],
+                               cudaStream_t s);
+
+/*
+ * ra_get_device_status -- synchronise stream s, then read and clear the
+ * current device's status word.  Returns RA_OK, the first error a kernel
+ * recorded since the last call, or RA_ERR_CUDA if the stream reported an
+ * asynchronous CUDA error.
+ */
+ra_status ra_get_device_status(cudaStream_t s);
+
+/* Static English name of a status code (never NULL). */
+const char *ra_status_string(ra_status st);
+
+/* Reason for the last non-OK status returned on this host thread (never NULL). */
+const char *ra_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ROPE_ATTN_H */

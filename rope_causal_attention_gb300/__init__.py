@@ -1,0 +1,221 @@
+"""Python binding of librope_attn.so (RoPE and causal attention with RoPE
+fused in, for GB300 / sm_103a).
+
+The functions mirror the C ABI in ``include/rope_attn.h`` one for one and do
+argument marshalling only: every step of the computation runs in the
+library's CUDA kernels.  PyTorch supplies device memory and the current
+stream.  There is no CPU path: a missing library or a non-CUDA tensor raises.
+
+Layouts: ``NEOX`` rotates pairs (i, i + rot_dim/2); ``GPTJ`` rotates pairs
+(2i, 2i+1) ("Write Triton Rope Kernel", Inputs the agent should gather
+first, item 1).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = ["NEOX", "GPTJ", "RAError", "rope_tables_build", "make_tables", "rope_apply_qk",
+           "attn_fwd_causal_rope", "ra_get_device_status", "ra_status_string", "library_path",
+           "lib"]
+
+NEOX = 0
+GPTJ = 1
+_DT = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_build", "librope_attn.so")
+_lock = threading.Lock()
+_lib = None
+
+_i64p = ctypes.POINTER(ctypes.c_int64)
+
+
+class RAError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(msg)
+        self.code = code
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib():
+    """The loaded ctypes library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise ImportError(
+                    f"{_LIB_PATH} is missing: build it with "
+                    "`python -c 'import __graft_entry__ as g; g.build()'` (there is no CPU fallback)")
+            L = ctypes.CDLL(_LIB_PATH)
+            vp, i64, i32, f64, f32 = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+                                      ctypes.c_double, ctypes.c_float)
+            L.rope_tables_build.argtypes = [vp, vp, i64, i32, f64, i32, vp]
+            L.rope_tables_build.restype = i32
+            L.rope_apply_qk.argtypes = [vp, vp, vp, vp, i32, i64, i32, i32, i32, i32, i32,
+                                        _i64p, _i64p, _i64p, _i64p, vp, i32, vp, vp, i64, vp]
+            L.rope_apply_qk.restype = i32
+            L.attn_fwd_causal_rope.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i64, i64,
+                                               i32, i64, i32, i32, i32, vp, vp, i64, f32,
+                                               _i64p, _i64p, _i64p, _i64p, vp]
+            L.attn_fwd_causal_rope.restype = i32
+            L.ra_get_device_status.argtypes = [vp]
+            L.ra_get_device_status.restype = i32
+            L.ra_status_string.argtypes = [i32]
+            L.ra_status_string.restype = ctypes.c_char_p
+            L.ra_last_error.argtypes = []
+            L.ra_last_error.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+def ra_status_string(code: int) -> str:
+    return lib().ra_status_string(int(code)).decode()
+
+
+def _check(code: int, what: str):
+    if code != 0:
+        L = lib()
+        raise RAError(code, f"{what}: {L.ra_status_string(code).decode()} "
+                            f"({L.ra_last_error().decode()})")
+
+
+def _arr(vals):
+    return (ctypes.c_int64 * len(vals))(*[int(x) for x in vals])
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(device, stream):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _cuda(t, name):
+    if t is not None and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+
+
+def rope_tables_build(cos_out: torch.Tensor, sin_out: torch.Tensor, base: float,
+                      freq_dim: int = 0, stream=None):
+    """Fills fp32 tables [rows, rot_dim/2] with cos/sin(p * base^(-2i/F))."""
+    _cuda(cos_out, "cos_out")
+    _cuda(sin_out, "sin_out")
+    if (cos_out.dtype != torch.float32 or sin_out.shape != cos_out.shape or cos_out.dim() != 2
+            or not cos_out.is_contiguous() or not sin_out.is_contiguous()):
+        raise ValueError("tables must be contiguous fp32 [rows, rot_dim/2] of equal shape")
+    rows, half = cos_out.shape
+    _check(lib().rope_tables_build(_ptr(cos_out), _ptr(sin_out), rows, 2 * half, float(base),
+                                   int(freq_dim), _stream(cos_out.device, stream)),
+           "rope_tables_build")
+    return cos_out, sin_out
+
+
+def make_tables(rows: int, rot_dim: int, base: float, freq_dim: int = 0, device="cuda",
+                stream=None):
+    """Allocates and builds the cos/sin tables (fp32 [rows, rot_dim/2] each)."""
+    c = torch.empty((rows, rot_dim // 2), dtype=torch.float32, device=device)
+    s = torch.empty_like(c)
+    return rope_tables_build(c, s, base, freq_dim, stream)
+
+
+def rope_apply_qk(q, k, positions, cos, sin, rot_dim: int | None = None, layout: int = NEOX,
+                  q_out=None, k_out=None, stream=None):
+    """Rotates token-major q [T, Hq, D] and k [T, Hkv, D] (either may be None)
+    at positions[t] in one launch; in place unless q_out / k_out are given.
+    Returns (q result, k result)."""
+    ref = q if q is not None else k
+    if ref is None:
+        raise ValueError("q or k required")
+    for t, n in ((q, "q"), (k, "k"), (q_out, "q_out"), (k_out, "k_out"), (positions, "positions"),
+                 (cos, "cos"), (sin, "sin")):
+        _cuda(t, n)
+    if positions.dtype not in (torch.int32, torch.int64) or positions.dim() != 1:
+        raise ValueError("positions must be int32 or int64 [T]")
+    T, _, D = ref.shape
+    for t, n in ((q, "q"), (k, "k"), (q_out, "q_out"), (k_out, "k_out")):
+        if t is not None and (t.dim() != 3 or t.shape[0] != T or t.shape[2] != D
+                              or t.stride(2) != 1 or t.dtype != ref.dtype):
+            raise ValueError(f"{n} must be [T, H, D] of one dtype with unit last stride")
+    if q_out is not None and q is not None and q_out.shape != q.shape:
+        raise ValueError("q_out shape must equal q's")
+    if k_out is not None and k is not None and k_out.shape != k.shape:
+        raise ValueError("k_out shape must equal k's")
+    if positions.shape[0] != T:
+        raise ValueError("one position per token required")
+    if cos.dtype != torch.float32 or cos.shape != sin.shape or not cos.is_contiguous():
+        raise ValueError("tables must be contiguous fp32 of equal shape")
+    rot_dim = 2 * cos.shape[1] if rot_dim is None else int(rot_dim)
+    if rot_dim != 2 * cos.shape[1]:
+        raise ValueError("rot_dim must match the table width (rot_dim/2 columns)")
+    Hq = q.shape[1] if q is not None else 0
+    Hkv = k.shape[1] if k is not None else 0
+    st = lambda t: _arr([t.stride(0), t.stride(1)]) if t is not None else None
+    _check(lib().rope_apply_qk(
+        _ptr(q), _ptr(k), _ptr(q_out), _ptr(k_out), _DT[ref.dtype], T, Hq, Hkv, D, rot_dim,
+        int(layout), st(q), st(k), st(q_out), st(k_out), _ptr(positions),
+        int(positions.dtype == torch.int64), _ptr(cos), _ptr(sin), cos.shape[0],
+        _stream(ref.device, stream)), "rope_apply_qk")
+    return (q_out if q_out is not None else q), (k_out if k_out is not None else k)
+
+
+def attn_fwd_causal_rope(q, k, v, cos=None, sin=None, kv_offset: int = 0, apply_rope: bool = True,
+                         rot_dim: int | None = None, layout: int = NEOX,
+                         softmax_scale: float | None = None, out=None, lse=None,
+                         return_lse: bool = True, stream=None):
+    """Causal attention forward with RoPE fused in.  q [B,Hq,Sq,D];
+    k, v [B,Hkv,Sk,D]; query row i sits at position kv_offset + i, key j at j.
+    Returns (O [B,Hq,Sq,D] in q's dtype, LSE fp32 [B,Hq,Sq] or None)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (cos, "cos"), (sin, "sin"), (out, "out"),
+                 (lse, "lse")):
+        _cuda(t, n)
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be 4-D [B, H, S, D]")
+    B, Hq, Sq, D = q.shape
+    _, Hkv, Sk, _ = k.shape
+    if k.shape != (B, Hkv, Sk, D) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, Hkv, Sk, D] with q's B and D")
+    if not (q.dtype == k.dtype == v.dtype) or q.dtype not in _DT:
+        raise ValueError("q, k, v must share one of fp32 / bf16 / fp16")
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        if t.stride(3) != 1:
+            raise ValueError(f"{n} needs unit stride in the head dimension")
+    if out is None:
+        out = torch.empty((B, Hq, Sq, D), dtype=q.dtype, device=q.device)
+    elif out.shape != (B, Hq, Sq, D) or out.dtype != q.dtype or out.stride(3) != 1:
+        raise ValueError("out must be [B, Hq, Sq, D] in q's dtype with unit last stride")
+    if return_lse and lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    if lse is not None and (lse.shape != (B, Hq, Sq) or lse.dtype != torch.float32
+                            or not lse.is_contiguous()):
+        raise ValueError("lse must be contiguous fp32 [B, Hq, Sq]")
+    if apply_rope:
+        if cos is None or sin is None:
+            raise ValueError("apply_rope needs the cos/sin tables")
+        rot_dim = 2 * cos.shape[1] if rot_dim is None else int(rot_dim)
+        if rot_dim != 2 * cos.shape[1]:
+            raise ValueError("rot_dim must match the table width")
+        rows = cos.shape[0]
+    else:
+        rot_dim, rows = D, 0
+    s3 = lambda t: _arr([t.stride(0), t.stride(1), t.stride(2)])
+    _check(lib().attn_fwd_causal_rope(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _DT[q.dtype], B, Hq, Hkv, Sq, Sk, D,
+        int(kv_offset), int(bool(apply_rope)), rot_dim, int(layout), _ptr(cos), _ptr(sin), rows,
+        float(softmax_scale) if softmax_scale is not None else 0.0, s3(q), s3(k), s3(v), s3(out),
+        _stream(q.device, stream)), "attn_fwd_causal_rope")
+    return out, lse
+
+
+def ra_get_device_status(stream=None, device=None) -> int:
+    """Synchronises the stream and returns (and clears) the device status code."""
+    return int(lib().ra_get_device_status(_stream(device, stream)))

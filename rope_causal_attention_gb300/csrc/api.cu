@@ -1,0 +1,331 @@
+// extern "C" entry points of librope_attn.so (declared in include/rope_attn.h):
+// host-side argument validation, the per-device status word and kernel
+// dispatch.  Every check runs before the first CUDA call, so a rejected call
+// touches no device state.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "internal.h"
+
+namespace {
+
+// First error recorded by any kernel on this device since the last read.
+__device__ int g_ra_status_word;
+
+thread_local char g_last_error[512] = "no error";
+
+constexpr int kMaxDevices = 64;
+std::mutex g_status_mu;
+int *g_status_ptr[kMaxDevices];
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t dtype_size(ra_dtype dt) { return dt == RA_F32 ? 4 : 2; }
+bool dtype_ok(int dt) { return dt == RA_F32 || dt == RA_BF16 || dt == RA_F16; }
+bool layout_ok(int l) { return l == RA_NEOX || l == RA_GPTJ; }
+
+// Byte footprint of a [n0][n1][D] strided array (strides in elements, >= 0).
+struct Region {
+  const char *base;
+  int64_t span;  // bytes from base to one past the last element
+  int64_t ts;    // outer (token) stride in bytes
+  int64_t foot;  // bytes covered by one outer index
+};
+
+Region region(const void *p, int64_t n0, int64_t s0, int64_t n1, int64_t s1, int64_t D, size_t es) {
+  Region r;
+  r.base = static_cast<const char *>(p);
+  r.foot = ((n1 - 1) * s1 + D) * (int64_t)es;
+  r.span = (n0 - 1) * s0 * (int64_t)es + r.foot;
+  r.ts = s0 * (int64_t)es;
+  return r;
+}
+
+// True when the two strided regions provably share no byte: disjoint spans,
+// or equal outer strides with per-row windows that do not meet (e.g. the q
+// and k slices of one packed qkv buffer).
+bool disjoint(const Region &a, const Region &b) {
+  if (a.base + a.span <= b.base || b.base + b.span <= a.base) return true;
+  if (a.ts != b.ts || a.ts <= 0 || a.foot > a.ts || b.foot > b.ts) return false;
+  const Region &x = a.base <= b.base ? a : b;
+  const Region &y = a.base <= b.base ? b : a;
+  const int64_t r = (int64_t)(y.base - x.base) % x.ts;
+  return x.foot <= r && r + y.foot <= x.ts;
+}
+
+}  // namespace
+
+namespace ra {
+
+ra_status fail(ra_status st, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+int *device_status_ptr(cudaError_t *err) {
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= kMaxDevices) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lk(g_status_mu);
+  if (!g_status_ptr[dev]) {
+    void *p = nullptr;
+    *err = cudaGetSymbolAddress(&p, g_ra_status_word);
+    if (*err != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<int *>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+}  // namespace ra
+
+using ra::fail;
+
+static ra_status cuda_fail(cudaError_t e, const char *what) {
+  return fail(RA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+extern "C" {
+
+const char *ra_status_string(ra_status st) {
+  switch (st) {
+    case RA_OK: return "RA_OK";
+    case RA_ERR_INVALID_ARG: return "RA_ERR_INVALID_ARG: invalid argument";
+    case RA_ERR_UNSUPPORTED: return "RA_ERR_UNSUPPORTED: no kernel for this case";
+    case RA_ERR_ALIGNMENT: return "RA_ERR_ALIGNMENT: misaligned pointer or stride";
+    case RA_ERR_OVERLAP: return "RA_ERR_OVERLAP: output overlaps an input";
+    case RA_ERR_CUDA: return "RA_ERR_CUDA: CUDA runtime error";
+    case RA_ERR_DEVICE_TIMEOUT: return "RA_ERR_DEVICE_TIMEOUT: kernel barrier wait timed out";
+    case RA_ERR_POSITION_RANGE: return "RA_ERR_POSITION_RANGE: position outside the cos/sin table";
+  }
+  return "unknown ra_status";
+}
+
+const char *ra_last_error(void) { return g_last_error; }
+
+ra_status rope_tables_build(float *cos_out, float *sin_out, int64_t rows, int rot_dim,
+                            double base, int freq_dim, cudaStream_t s) {
+  if (rows < 0) return fail(RA_ERR_INVALID_ARG, "rows must be >= 0 (got %lld)", (long long)rows);
+  if (rot_dim < 2 || (rot_dim & 1))
+    return fail(RA_ERR_INVALID_ARG, "rot_dim must be even and >= 2 (got %d)", rot_dim);
+  if (!(base > 0.0) || !isfinite(base))
+    return fail(RA_ERR_INVALID_ARG, "base must be finite and > 0");
+  if (freq_dim < 0) return fail(RA_ERR_INVALID_ARG, "freq_dim must be >= 0");
+  if (rows > 0 && (!cos_out || !sin_out)) return fail(RA_ERR_INVALID_ARG, "null table pointer");
+  if (!aligned(cos_out, 4) || !aligned(sin_out, 4))
+    return fail(RA_ERR_ALIGNMENT, "tables must be 4-byte aligned");
+  if (rows == 0) return RA_OK;
+  const ra::TableArgs a{cos_out, sin_out, rows, rot_dim, freq_dim, base};
+  const cudaError_t e = ra::launch_table_build(a, s);
+  return e == cudaSuccess ? RA_OK : cuda_fail(e, "rope_tables_build launch");
+}
+
+ra_status rope_apply_qk(void *q, void *k, void *q_out, void *k_out, ra_dtype dt, int64_t T,
+                        int Hq, int Hkv, int D, int rot_dim, ra_layout layout,
+                        const int64_t strides_q[2], const int64_t strides_k[2],
+                        const int64_t strides_qo[2], const int64_t strides_ko[2],
+                        const void *positions, int pos_is_int64, const float *cos_t,
+                        const float *sin_t, int64_t table_rows, cudaStream_t s) {
+  if (!dtype_ok(dt)) return fail(RA_ERR_INVALID_ARG, "unknown dtype %d", (int)dt);
+  if (!layout_ok(layout)) return fail(RA_ERR_INVALID_ARG, "unknown layout %d", (int)layout);
+  if (T < 0 || Hq < 0 || Hkv < 0) return fail(RA_ERR_INVALID_ARG, "T, Hq, Hkv must be >= 0");
+  if (D < 2 || (D & 1)) return fail(RA_ERR_INVALID_ARG, "D must be even and >= 2 (got %d)", D);
+  if (rot_dim < 2 || (rot_dim & 1) || rot_dim > D)
+    return fail(RA_ERR_INVALID_ARG, "rot_dim must be even with 2 <= rot_dim <= D (got %d)", rot_dim);
+  if ((Hq > 0) != (q != nullptr) || (Hkv > 0) != (k != nullptr))
+    return fail(RA_ERR_INVALID_ARG, "q (k) must be non-NULL exactly when Hq (Hkv) > 0");
+  if (table_rows < 1) return fail(RA_ERR_INVALID_ARG, "table_rows must be >= 1");
+  if (!positions || !cos_t || !sin_t)
+    return fail(RA_ERR_INVALID_ARG, "positions and tables must be non-NULL");
+  const bool qin = q_out == nullptr || q_out == q;
+  const bool kin = k_out == nullptr || k_out == k;
+  if ((Hq > 0 && !strides_q) || (Hkv > 0 && !strides_k) || (Hq > 0 && !qin && !strides_qo) ||
+      (Hkv > 0 && !kin && !strides_ko))
+    return fail(RA_ERR_INVALID_ARG, "stride arrays must be non-NULL for every tensor used");
+  const int64_t zero2[2] = {0, 0};
+  const int64_t *sq = Hq > 0 ? strides_q : zero2, *sk = Hkv > 0 ? strides_k : zero2;
+  const int64_t *sqo = (Hq > 0 && !qin) ? strides_qo : sq;
+  const int64_t *sko = (Hkv > 0 && !kin) ? strides_ko : sk;
+  for (int j = 0; j < 2; ++j)
+    if (sq[j] < 0 || sk[j] < 0 || sqo[j] < 0 || sko[j] < 0)
+      return fail(RA_ERR_INVALID_ARG, "strides must be >= 0");
+  if (T == 0 || Hq + Hkv == 0) return RA_OK;
+
+  const size_t es = dtype_size(dt);
+  // overlap rules: an output equals its input or shares no byte with any input/output
+  if (Hq > 0 && Hkv > 0) {
+    const Region rq = region(q, T, sq[0], Hq, sq[1], D, es);
+    const Region rk = region(k, T, sk[0], Hkv, sk[1], D, es);
+    const Region rqo = region(qin ? q : q_out, T, sqo[0], Hq, sqo[1], D, es);
+    const Region rko = region(kin ? k : k_out, T, sko[0], Hkv, sko[1], D, es);
+    if (!disjoint(rqo, rk) || !disjoint(rko, rq) || !disjoint(rqo, rko))
+      return fail(RA_ERR_OVERLAP, "q/k outputs overlap the other tensor");
+  }
+  if (Hq > 0 && !qin &&
+      !disjoint(region(q, T, sq[0], Hq, sq[1], D, es), region(q_out, T, sqo[0], Hq, sqo[1], D, es)))
+    return fail(RA_ERR_OVERLAP, "q_out partially overlaps q");
+  if (Hkv > 0 && !kin &&
+      !disjoint(region(k, T, sk[0], Hkv, sk[1], D, es), region(k_out, T, sko[0], Hkv, sko[1], D, es)))
+    return fail(RA_ERR_OVERLAP, "k_out partially overlaps k");
+
+  if (!aligned(positions, pos_is_int64 ? 8 : 4) || !aligned(cos_t, 4) || !aligned(sin_t, 4))
+    return fail(RA_ERR_ALIGNMENT, "positions/tables misaligned");
+  const void *ptrs[4] = {q, k, qin ? q : q_out, kin ? k : k_out};
+  for (const void *p : ptrs)
+    if (p && !aligned(p, es)) return fail(RA_ERR_ALIGNMENT, "q/k buffers must be element-aligned");
+
+  // vector path: 16-byte aligned pointers, strides, pair offsets and tail
+  const int V = (int)(16 / es);
+  const int half = rot_dim / 2;
+  bool vec = aligned(cos_t, 16) && aligned(sin_t, 16);
+  for (const void *p : ptrs) vec = vec && (!p || aligned(p, 16));
+  for (int j = 0; j < 2; ++j)
+    vec = vec && sq[j] % V == 0 && sk[j] % V == 0 && sqo[j] % V == 0 && sko[j] % V == 0;
+  vec = vec && (layout == RA_NEOX ? half % V == 0 : rot_dim % V == 0);
+  const bool copy_tail = !(qin && kin);
+  if (copy_tail) vec = vec && (D - rot_dim) % V == 0;
+  const int slices = (layout == RA_NEOX ? half / V : rot_dim / V) + (copy_tail ? (D - rot_dim) / V : 0);
+  vec = vec && slices >= 1 && slices <= 1024;
+
+  cudaError_t e;
+  int *status = ra::device_status_ptr(&e);
+  if (!status) return cuda_fail(e, "status word");
+  ra::RopeArgs a{};
+  a.q = q; a.k = k; a.q_out = q_out; a.k_out = k_out; a.dt = dt; a.T = T; a.Hq = Hq;
+  a.Hkv = Hkv; a.D = D; a.rot_dim = rot_dim; a.layout = layout;
+  for (int j = 0; j < 2; ++j) {
+    a.sq[j] = sq[j]; a.sk[j] = sk[j]; a.sqo[j] = sqo[j]; a.sko[j] = sko[j];
+  }
+  a.positions = positions; a.pos_is_int64 = pos_is_int64 ? 1 : 0;
+  a.cos_t = cos_t; a.sin_t = sin_t; a.table_rows = table_rows; a.status = status;
+  e = ra::launch_rope_apply(a, vec, s);
+  return e == cudaSuccess ? RA_OK : cuda_fail(e, "rope_apply_qk launch");
+}
+
+ra_status attn_fwd_causal_rope(const void *q, const void *k, const void *v, void *o, float *lse,
+                               ra_dtype dt, int B, int Hq, int Hkv, int64_t Sq, int64_t Sk,
+                               int D, int64_t kv_offset, int apply_rope, int rot_dim,
+                               ra_layout layout, const float *cos_t, const float *sin_t,
+                               int64_t table_rows, float softmax_scale,
+                               const int64_t strides_q[3], const int64_t strides_k[3],
+                               const int64_t strides_v[3], const int64_t strides_o[3],
+                               cudaStream_t s) {
+  if (!dtype_ok(dt)) return fail(RA_ERR_INVALID_ARG, "unknown dtype %d", (int)dt);
+  if (B < 1 || Hq < 1 || Hkv < 1) return fail(RA_ERR_INVALID_ARG, "B, Hq, Hkv must be >= 1");
+  if (Hq % Hkv) return fail(RA_ERR_INVALID_ARG, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
+  if (Sq < 0 || Sk < 1) return fail(RA_ERR_INVALID_ARG, "need Sq >= 0 and Sk >= 1");
+  if (kv_offset < 0)
+    return fail(RA_ERR_INVALID_ARG, "kv_offset must be >= 0: a negative offset leaves query rows "
+                                    "with no admissible key");
+  if (D < 2 || (D & 1)) return fail(RA_ERR_INVALID_ARG, "D must be even and >= 2");
+  if (!q || !k || !v || !o) return fail(RA_ERR_INVALID_ARG, "q, k, v, o must be non-NULL");
+  if (!strides_q || !strides_k || !strides_v || !strides_o)
+    return fail(RA_ERR_INVALID_ARG, "stride arrays must be non-NULL");
+  for (int j = 0; j < 3; ++j)
+    if (strides_q[j] < 0 || strides_k[j] < 0 || strides_v[j] < 0 || strides_o[j] < 0)
+      return fail(RA_ERR_INVALID_ARG, "strides must be >= 0");
+  if (apply_rope) {
+    if (!layout_ok(layout)) return fail(RA_ERR_INVALID_ARG, "unknown layout %d", (int)layout);
+    if (rot_dim < 2 || (rot_dim & 1) || rot_dim > D)
+      return fail(RA_ERR_INVALID_ARG, "rot_dim must be even with 2 <= rot_dim <= D");
+    if (!cos_t || !sin_t) return fail(RA_ERR_INVALID_ARG, "tables must be non-NULL");
+    const int64_t need = Sk > kv_offset + Sq ? Sk : kv_offset + Sq;
+    if (table_rows < need)
+      return fail(RA_ERR_INVALID_ARG, "table_rows %lld < needed %lld", (long long)table_rows,
+                  (long long)need);
+    if (!aligned(cos_t, 16) || !aligned(sin_t, 16))
+      return fail(RA_ERR_ALIGNMENT, "tables must be 16-byte aligned");
+  }
+  if (!(softmax_scale <= 0.f) && !isfinite(softmax_scale))
+    return fail(RA_ERR_INVALID_ARG, "softmax_scale must be finite");
+  if (Sq == 0) return RA_OK;
+  const size_t es = dtype_size(dt);
+  if (!aligned(q, es) || !aligned(k, es) || !aligned(v, es) || !aligned(o, es) ||
+      (lse && !aligned(lse, 4)))
+    return fail(RA_ERR_ALIGNMENT, "buffers must be element-aligned");
+  // the output must not overlap any input
+  {
+    const char *ob = static_cast<const char *>(o);
+    const int64_t ospan = (((int64_t)B - 1) * strides_o[0] + ((int64_t)Hq - 1) * strides_o[1] +
+                           (Sq - 1) * strides_o[2] + D) * (int64_t)es;
+    const void *ins[3] = {q, k, v};
+    const int64_t *sts[3] = {strides_q, strides_k, strides_v};
+    const int64_t heads[3] = {Hq, Hkv, Hkv};
+    const int64_t lens[3] = {Sq, Sk, Sk};
+    for (int t = 0; t < 3; ++t) {
+      const char *ib = static_cast<const char *>(ins[t]);
+      const int64_t ispan = (((int64_t)B - 1) * sts[t][0] + (heads[t] - 1) * sts[t][1] +
+                             (lens[t] - 1) * sts[t][2] + D) * (int64_t)es;
+      if (!(ob + ospan <= ib || ib + ispan <= ob))
+        return fail(RA_ERR_OVERLAP, "o overlaps an input");
+    }
+    if (lse) {
+      const char *lb = reinterpret_cast<const char *>(lse);
+      const int64_t lspan = (int64_t)B * Hq * Sq * 4;
+      if (!(lb + lspan <= ob || ob + ospan <= lb)) return fail(RA_ERR_OVERLAP, "lse overlaps o");
+    }
+  }
+
+  ra::AttnArgs a{};
+  a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse; a.dt = dt;
+  a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.Sq = Sq; a.Sk = Sk; a.D = D; a.kv_offset = kv_offset;
+  a.apply_rope = apply_rope ? 1 : 0;
+  a.rot_dim = apply_rope ? rot_dim : D;
+  a.layout = layout_ok(layout) ? layout : RA_NEOX;
+  a.cos_t = cos_t; a.sin_t = sin_t; a.table_rows = table_rows;
+  a.scale = softmax_scale > 0.f ? softmax_scale : (float)(1.0 / sqrt((double)D));
+  for (int j = 0; j < 3; ++j) {
+    a.sq[j] = strides_q[j]; a.sk[j] = strides_k[j]; a.sv[j] = strides_v[j]; a.so[j] = strides_o[j];
+  }
+
+  if (dt == RA_F32) {
+    if (D > 256) return fail(RA_ERR_UNSUPPORTED, "fp32 attention supports D <= 256 (got %d)", D);
+    cudaError_t e;
+    a.status = ra::device_status_ptr(&e);
+    if (!a.status) return cuda_fail(e, "status word");
+    e = ra::launch_attn_simt(a, s);
+    return e == cudaSuccess ? RA_OK : cuda_fail(e, "attention (fp32) launch");
+  }
+  if (D != 64 && D != 128)
+    return fail(RA_ERR_UNSUPPORTED, "tensor-core attention supports D in {64, 128} (got %d)", D);
+  if (apply_rope && (layout == RA_NEOX ? (rot_dim / 2) % 8 : rot_dim % 8))
+    return fail(RA_ERR_UNSUPPORTED, "tensor-core attention needs rot_dim/2 %% 8 == 0 (NeoX) or "
+                                    "rot_dim %% 8 == 0 (GPT-J)");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+    return fail(RA_ERR_ALIGNMENT, "tensor-core attention needs 16-byte aligned q, k, v, o");
+  for (int j = 0; j < 3; ++j)
+    if (strides_q[j] % 8 || strides_k[j] % 8 || strides_v[j] % 8 || strides_o[j] % 8)
+      return fail(RA_ERR_ALIGNMENT, "tensor-core attention needs strides that are multiples of 8");
+  cudaError_t e;
+  a.status = ra::device_status_ptr(&e);
+  if (!a.status) return cuda_fail(e, "status word");
+  e = ra::launch_attn_tc(a, s);
+  if (e == cudaErrorNotSupported) return fail(RA_ERR_UNSUPPORTED, "no tensor-core variant");
+  return e == cudaSuccess ? RA_OK : cuda_fail(e, "attention (tensor core) launch");
+}
+
+ra_status ra_get_device_status(cudaStream_t s) {
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  int v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_ra_status_word, sizeof v);
+  if (e != cudaSuccess) return cuda_fail(e, "read status word");
+  const int zero = 0;
+  e = cudaMemcpyToSymbol(g_ra_status_word, &zero, sizeof zero);
+  if (e != cudaSuccess) return cuda_fail(e, "clear status word");
+  if (v == 0) return RA_OK;
+  return fail((ra_status)v, "device reported %s", ra_status_string((ra_status)v));
+}
+
+}  // extern "C"

@@ -1,0 +1,200 @@
+// fp32 causal attention with RoPE fused in, on CUDA cores.
+//
+// Serves fp32 inputs, where rounding rotated Q/K to a 16-bit tensor-core
+// operand would break a 1e-4 output tolerance.  Same mathematics as the
+// tensor-core kernel ("RoPE and FlashAttention: relative positions and online
+// softmax", sections 1, 2, 4, 5): Q rotated once at kv_offset + i, each K tile
+// rotated as it is staged in shared memory, online softmax with running max m,
+// denominator l and numerator u, output u / l, LSE = m + ln l.
+//
+// Layout: one warp per query row (lanes split the head dimension, D <= 256),
+// eight rows per block, key tiles of 32 rows staged (rotated) in shared
+// memory and shared by the eight warps.  Lane j of a warp holds the score of
+// key j of the tile, so the tile's softmax statistics are warp reductions.
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace ra {
+namespace {
+
+constexpr int kRows = 8;    // query rows (warps) per block
+constexpr int kTileK = 32;  // keys per staged tile (one per lane)
+constexpr int kMaxPerLane = 8;  // D <= 256
+
+struct SimtParams {
+  const float *q, *k, *v;
+  float *o, *lse;
+  int Hq, G, D;
+  int64_t Sq, Sk, kv_offset;
+  int apply_rope, rot_dim, layout;
+  const float *cos_t, *sin_t;
+  float scale;
+  int64_t sq[3], sk[3], sv[3], so[3];
+};
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+// Rotated value of dim d of row x (fp32 values, length D) at position pos.
+__device__ __forceinline__ float rotated(const float *x, int d, int64_t pos, const SimtParams &p) {
+  if (!p.apply_rope || d >= p.rot_dim) return x[d];
+  const int half = p.rot_dim >> 1;
+  int i, partner;
+  bool low;
+  if (p.layout == RA_NEOX) {
+    low = d < half;
+    i = low ? d : d - half;
+    partner = low ? d + half : d - half;
+  } else {
+    low = (d & 1) == 0;
+    i = d >> 1;
+    partner = low ? d + 1 : d - 1;
+  }
+  const float c = __ldg(p.cos_t + pos * half + i);
+  const float s = __ldg(p.sin_t + pos * half + i);
+  return low ? x[d] * c - x[partner] * s : x[d] * c + x[partner] * s;
+}
+
+__global__ void __launch_bounds__(kRows * 32) attn_simt_kernel(SimtParams p) {
+  extern __shared__ float smem[];
+  const int D = p.D;
+  float *sK = smem;                      // [kTileK][D] rotated keys
+  float *sV = sK + kTileK * D;           // [kTileK][D]
+  float *sRaw = sV + kTileK * D;         // [kTileK][D] raw keys, then per-warp q rows
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y, b = blockIdx.z, hk = h / p.G;
+  const int64_t i = (int64_t)blockIdx.x * kRows + warp;  // this warp's query row
+  const bool row_ok = i < p.Sq;
+  const int64_t qpos = p.kv_offset + i;
+
+  // ---- rotate this warp's query row once
+  float qr[kMaxPerLane];
+  {
+    float *xr = sRaw + warp * D;
+    if (row_ok) {
+      const float *src = p.q + b * p.sq[0] + h * p.sq[1] + i * p.sq[2];
+      for (int d = lane; d < D; d += 32) xr[d] = src[d];
+    }
+    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < kMaxPerLane; ++u) {
+      const int d = lane + 32 * u;
+      qr[u] = (row_ok && d < D) ? rotated(xr, d, qpos, p) : 0.f;
+    }
+  }
+  __syncthreads();
+
+  float m = -INFINITY, l = 0.f, acc[kMaxPerLane];
+#pragma unroll
+  for (int u = 0; u < kMaxPerLane; ++u) acc[u] = 0.f;
+
+  const int64_t last_row = min((int64_t)blockIdx.x * kRows + kRows - 1, p.Sq - 1);
+  const int64_t kend = min(p.Sk, p.kv_offset + last_row + 1);
+  const float *kb = p.k + b * p.sk[0] + hk * p.sk[1];
+  const float *vb = p.v + b * p.sv[0] + hk * p.sv[1];
+
+  for (int64_t j0 = 0; j0 < kend; j0 += kTileK) {
+    const int nk = (int)min((int64_t)kTileK, kend - j0);
+    // stage raw K and V
+    for (int e = threadIdx.x; e < kTileK * D; e += blockDim.x) {
+      const int jj = e / D, d = e - jj * D;
+      float kx = 0.f, vx = 0.f;
+      if (jj < nk) {
+        kx = kb[(j0 + jj) * p.sk[2] + d];
+        vx = vb[(j0 + jj) * p.sv[2] + d];
+      }
+      sRaw[e] = kx;
+      sV[e] = vx;
+    }
+    __syncthreads();
+    // rotate K at positions j
+    for (int e = threadIdx.x; e < kTileK * D; e += blockDim.x) {
+      const int jj = e / D, d = e - jj * D;
+      sK[e] = jj < nk ? rotated(sRaw + jj * D, d, j0 + jj, p) : 0.f;
+    }
+    __syncthreads();
+
+    if (row_ok) {
+      float my_s = -INFINITY;
+      for (int jj = 0; jj < kTileK; ++jj) {
+        float part = 0.f;
+#pragma unroll
+        for (int u = 0; u < kMaxPerLane; ++u) {
+          const int d = lane + 32 * u;
+          if (d < D) part += qr[u] * sK[jj * D + d];
+        }
+        part = warp_sum(part);
+        const int64_t j = j0 + jj;
+        if (lane == jj && jj < nk && j <= qpos) my_s = part * p.scale;
+      }
+      const float tmax = warp_max(my_s);
+      if (tmax != -INFINITY) {
+        const float m_new = fmaxf(m, tmax);
+        const float corr = expf(m - m_new);
+        const float pj = expf(my_s - m_new);
+        l = l * corr + warp_sum(pj);
+#pragma unroll
+        for (int u = 0; u < kMaxPerLane; ++u) acc[u] *= corr;
+        for (int jj = 0; jj < nk; ++jj) {
+          const float w = __shfl_sync(0xffffffffu, pj, jj);
+#pragma unroll
+          for (int u = 0; u < kMaxPerLane; ++u) {
+            const int d = lane + 32 * u;
+            if (d < D) acc[u] += w * sV[jj * D + d];
+          }
+        }
+        m = m_new;
+      }
+    }
+    __syncthreads();
+  }
+
+  if (row_ok) {
+    const float inv = 1.f / l;
+    float *dst = p.o + b * p.so[0] + h * p.so[1] + i * p.so[2];
+#pragma unroll
+    for (int u = 0; u < kMaxPerLane; ++u) {
+      const int d = lane + 32 * u;
+      if (d < D) dst[d] = acc[u] * inv;
+    }
+    if (p.lse && lane == 0) p.lse[((int64_t)b * p.Hq + h) * p.Sq + i] = m + logf(l);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_attn_simt(const AttnArgs &a, cudaStream_t s) {
+  SimtParams p{};
+  p.q = static_cast<const float *>(a.q);
+  p.k = static_cast<const float *>(a.k);
+  p.v = static_cast<const float *>(a.v);
+  p.o = static_cast<float *>(a.o);
+  p.lse = a.lse;
+  p.Hq = a.Hq; p.G = a.Hq / a.Hkv; p.D = a.D;
+  p.Sq = a.Sq; p.Sk = a.Sk; p.kv_offset = a.kv_offset;
+  p.apply_rope = a.apply_rope; p.rot_dim = a.rot_dim; p.layout = a.layout;
+  p.cos_t = a.cos_t; p.sin_t = a.sin_t; p.scale = a.scale;
+  for (int j = 0; j < 3; ++j) {
+    p.sq[j] = a.sq[j]; p.sk[j] = a.sk[j]; p.sv[j] = a.sv[j]; p.so[j] = a.so[j];
+  }
+  const size_t smem = (size_t)3 * kTileK * a.D * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(attn_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((unsigned)((a.Sq + kRows - 1) / kRows), (unsigned)a.Hq, (unsigned)a.B);
+  attn_simt_kernel<<<grid, kRows * 32, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace ra

@@ -1,0 +1,65 @@
+// Internal declarations shared by the translation units of librope_attn.so.
+// Not part of the C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/rope_attn.h"
+
+namespace ra {
+
+// Status word of the current device (a __device__ int in api.cu).  Kernels
+// record the first error with atomicCAS(status, 0, code).
+int *device_status_ptr(cudaError_t *err);
+
+// Records a readable reason for the current host thread and returns st.
+ra_status fail(ra_status st, const char *fmt, ...);
+
+struct TableArgs {
+  float *cos_out, *sin_out;
+  int64_t rows;
+  int rot_dim, freq_dim;
+  double base;
+};
+
+struct RopeArgs {
+  void *q, *k, *q_out, *k_out;
+  ra_dtype dt;
+  int64_t T;
+  int Hq, Hkv, D, rot_dim;
+  ra_layout layout;
+  int64_t sq[2], sk[2], sqo[2], sko[2];
+  const void *positions;
+  int pos_is_int64;
+  const float *cos_t, *sin_t;
+  int64_t table_rows;
+  int *status;
+};
+
+struct AttnArgs {
+  const void *q, *k, *v;
+  void *o;
+  float *lse;
+  ra_dtype dt;
+  int B, Hq, Hkv;
+  int64_t Sq, Sk;
+  int D;
+  int64_t kv_offset;
+  int apply_rope, rot_dim;
+  ra_layout layout;
+  const float *cos_t, *sin_t;
+  int64_t table_rows;
+  float scale;
+  int64_t sq[3], sk[3], sv[3], so[3];
+  int *status;
+};
+
+cudaError_t launch_table_build(const TableArgs &a, cudaStream_t s);
+cudaError_t launch_rope_apply(const RopeArgs &a, bool vectorized, cudaStream_t s);
+cudaError_t launch_attn_simt(const AttnArgs &a, cudaStream_t s);
+// Returns cudaErrorNotSupported when the tensor-core kernel has no variant
+// for the case (the caller maps it to RA_ERR_UNSUPPORTED).
+cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t s);
+
+}  // namespace ra

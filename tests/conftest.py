@@ -34,3 +34,25 @@ def oracle_mod():
     import oracle
     oracle.build()
     return oracle
+
+
+def ordered_bits(t):
+    """Maps float tensors (CPU) to integers whose differences count ulps."""
+    import torch
+    if t.dtype == torch.float32:
+        i = t.contiguous().view(torch.int32).to(torch.int64)
+        mag = i & 0x7FFFFFFF
+    else:
+        i = t.contiguous().view(torch.int16).to(torch.int64)
+        mag = i & 0x7FFF
+    return torch.where(i < 0, -mag, mag)
+
+
+def ulp_distance(a, b):
+    """Elementwise distance in units in the last place of a's dtype."""
+    return (ordered_bits(a) - ordered_bits(b.to(a.dtype))).abs()
+
+
+def gpu_ready():
+    import torch
+    return torch.cuda.is_available()

@@ -1,0 +1,186 @@
+"""GPU parity: attn_fwd_causal_rope against the fp64 oracle.
+
+Tolerances (max absolute error against the fp64 result): O <= 2e-2 for
+bf16/fp16 inputs and <= 1e-4 for fp32 inputs; LSE <= 1e-3 for every dtype.
+Inputs are the seeded tensors of ``workloads``.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+NEOX, GPTJ = 0, 1
+TOL = {torch.float32: (1e-4, 1e-3), torch.bfloat16: (2e-2, 1e-3), torch.float16: (2e-2, 1e-3)}
+
+
+@pytest.fixture(scope="module")
+def ra():
+    import __graft_entry__
+    __graft_entry__.build()
+    import rope_causal_attention_gb300 as m
+    assert m.ra_get_device_status() == 0
+    return m
+
+
+@pytest.fixture(scope="module")
+def orc():
+    import oracle
+    oracle.build()
+    return oracle
+
+
+def run_case(ra, orc, dt, B, Hq, Hkv, Sq, Sk, D, off, layout=NEOX, rot_dim=None, apply_rope=True,
+             base=10000.0, seed=0, rows=None, scale=None, qkv=None, strided=False):
+    q, k, v = qkv if qkv is not None else wl.attn_qkv(B, Hq, Hkv, Sq, Sk, D, dt, seed)
+    r = rot_dim or D
+    cos = sin = None
+    if apply_rope:
+        cos, sin = ra.make_tables(max(Sk, off + Sq), r, base)
+    if strided:  # token-major [B, S, H, D] storage viewed as [B, H, S, D]
+        qg = q.transpose(1, 2).contiguous().cuda().transpose(1, 2)
+        kg = k.transpose(1, 2).contiguous().cuda().transpose(1, 2)
+        vg = v.transpose(1, 2).contiguous().cuda().transpose(1, 2)
+    else:
+        qg, kg, vg = q.cuda(), k.cuda(), v.cuda()
+    o, lse = ra.attn_fwd_causal_rope(qg, kg, vg, cos, sin, kv_offset=off, apply_rope=apply_rope,
+                                     rot_dim=r if apply_rope else None, layout=layout,
+                                     softmax_scale=scale)
+    assert ra.ra_get_device_status() == 0
+    o_ref, lse_ref = orc.attention(q.float().numpy(), k.float().numpy(), v.float().numpy(),
+                                   kv_offset=off, apply_rope=apply_rope, rot_dim=r, base=base,
+                                   layout=layout, scale=scale, rows=rows)
+    og = o.float().cpu().numpy().reshape(-1, D)
+    lg = lse.cpu().numpy().reshape(-1)
+    if rows is not None:
+        og, lg = og[rows], lg[rows]
+    else:
+        o_ref, lse_ref = o_ref.reshape(-1, D), lse_ref.reshape(-1)
+    eo = np.abs(og - o_ref).max()
+    el = np.abs(lg - lse_ref).max()
+    to, tl = TOL[dt]
+    assert np.isfinite(og).all() and np.isfinite(lg).all()
+    assert eo <= to and el <= tl, f"O err {eo:.3g} (tol {to}), LSE err {el:.3g} (tol {tl})"
+    return eo, el
+
+
+# ------------------------------------------------------------------ fp32 path
+def test_fp32_workload_full(ra, orc):
+    """fp32, B=1 H=2 S=128 D=64, NeoX, base 1e4, positions 0..127, scale 1/8."""
+    W = wl.FP32_ATTN
+    run_case(ra, orc, torch.float32, W.B, W.Hq, W.Hkv, W.Sq, W.Sk, W.D, W.kv_offset,
+             layout=W.layout, base=W.base, qkv=W.inputs(), scale=1 / 8)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Sk,D,off,layout,rot", [
+    (1, 4, 2, 37, 50, 64, 13, GPTJ, None),
+    (2, 2, 1, 70, 70, 32, 0, NEOX, 16),
+    (1, 3, 3, 1, 90, 128, 89, NEOX, None),
+    (1, 2, 1, 33, 33, 256, 0, GPTJ, 128),
+    (1, 1, 1, 5, 9, 6, 2, NEOX, 4),
+])
+def test_fp32_cases(ra, orc, B, Hq, Hkv, Sq, Sk, D, off, layout, rot):
+    run_case(ra, orc, torch.float32, B, Hq, Hkv, Sq, Sk, D, off, layout=layout, rot_dim=rot,
+             seed=Sq + D)
+
+
+def test_fp32_no_rope_matches_textbook(ra, orc):
+    run_case(ra, orc, torch.float32, 1, 2, 2, 40, 60, 64, 20, apply_rope=False, seed=3)
+
+
+# ------------------------------------------------------------ tensor-core path
+TC_CASES = [
+    # dt, B, Hq, Hkv, Sq, Sk, D, off, layout, rot
+    (torch.bfloat16, 1, 1, 1, 1, 1, 64, 0, NEOX, None),
+    (torch.bfloat16, 1, 2, 2, 128, 128, 64, 0, GPTJ, None),
+    (torch.bfloat16, 1, 2, 1, 130, 130, 64, 0, NEOX, None),
+    (torch.bfloat16, 2, 4, 2, 300, 300, 128, 0, NEOX, None),
+    (torch.bfloat16, 1, 4, 1, 77, 300, 128, 223, GPTJ, None),
+    (torch.bfloat16, 1, 8, 2, 200, 260, 128, 60, NEOX, 64),
+    (torch.bfloat16, 1, 2, 2, 256, 256, 64, 0, GPTJ, 32),
+    (torch.bfloat16, 1, 4, 4, 1, 1000, 128, 999, NEOX, None),
+    (torch.bfloat16, 1, 3, 1, 129, 1500, 64, 1371, GPTJ, None),
+    (torch.float16, 1, 4, 2, 190, 190, 128, 0, NEOX, None),
+    (torch.float16, 2, 2, 2, 65, 100, 64, 35, GPTJ, None),
+]
+
+
+@pytest.mark.parametrize("dt,B,Hq,Hkv,Sq,Sk,D,off,layout,rot", TC_CASES)
+def test_tensor_core_cases(ra, orc, dt, B, Hq, Hkv, Sq, Sk, D, off, layout, rot):
+    run_case(ra, orc, dt, B, Hq, Hkv, Sq, Sk, D, off, layout=layout, rot_dim=rot, seed=Sq * 3 + Sk)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_tensor_core_without_rope(ra, orc, D):
+    """apply_rope = 0: plain causal flash attention (also the path for a cache
+    of already-rotated keys)."""
+    run_case(ra, orc, torch.bfloat16, 1, 4, 2, 260, 300, D, 40, apply_rope=False, seed=D)
+
+
+def test_tensor_core_strided_token_major(ra, orc):
+    """Q/K/V stored token-major [B, S, H, D] and passed as [B, H, S, D] views."""
+    run_case(ra, orc, torch.bfloat16, 2, 4, 2, 150, 150, 128, 0, strided=True, seed=4)
+
+
+def test_tensor_core_custom_scale(ra, orc):
+    run_case(ra, orc, torch.bfloat16, 1, 2, 1, 140, 140, 64, 0, scale=0.3, seed=5)
+
+
+@pytest.mark.parametrize("W", wl.SWEEP, ids=[w.name for w in wl.SWEEP])
+def test_sweep_workloads_full(ra, orc, W):
+    """bf16 GPT-J sweep B x 8 x S x 64 (S 512..4096, B 1..4): every row."""
+    run_case(ra, orc, torch.bfloat16, W.B, W.Hq, W.Hkv, W.Sq, W.Sk, W.D, W.kv_offset,
+             layout=W.layout, base=W.base, qkv=W.inputs())
+
+
+def test_long_context_gqa_sampled_rows(ra, orc):
+    """bf16 GQA 32 q-heads / 8 kv-heads, Sq 16384 new queries after a 4096-row
+    cached prefix (Sk 20480), D 128, base 5e5, NeoX: full-size launch, checked
+    on 1024 seeded random rows plus the first and last 128 rows of heads 0
+    and 31."""
+    W = wl.LONG_GQA
+    rng = np.random.default_rng(77)
+    n = W.B * W.Hq * W.Sq
+    edge = []
+    for h in (0, W.Hq - 1):
+        base_row = h * W.Sq
+        edge += list(range(base_row, base_row + 128)) + list(range(base_row + W.Sq - 128,
+                                                                    base_row + W.Sq))
+    rows = np.unique(np.concatenate([rng.integers(0, n, 1024), np.array(edge)]))
+    run_case(ra, orc, torch.bfloat16, W.B, W.Hq, W.Hkv, W.Sq, W.Sk, W.D, W.kv_offset,
+             layout=W.layout, base=W.base, qkv=W.inputs(), rows=rows)
+
+
+def test_peak_extra_memory_bounded(ra):
+    """Peak extra device memory of one call (beyond inputs and tables) stays
+    within O + LSE: no rotated or expanded tensor is materialised."""
+    B, Hq, Hkv, S, D = 1, 8, 8, 2048, 64
+    q, k, v = [t.cuda() for t in wl.attn_qkv(B, Hq, Hkv, S, S, D, torch.bfloat16, 9)]
+    cos, sin = ra.make_tables(S, D, 10000.0)
+    torch.cuda.synchronize()
+    base = torch.cuda.memory_allocated()
+    torch.cuda.reset_peak_memory_stats()
+    o, lse = ra.attn_fwd_causal_rope(q, k, v, cos, sin)
+    torch.cuda.synchronize()
+    extra = torch.cuda.max_memory_allocated() - base
+    assert extra <= o.numel() * o.element_size() + lse.numel() * 4 + 1024
+
+
+def test_rejections_with_real_buffers(ra):
+    q, k, v = [t.cuda() for t in wl.attn_qkv(1, 2, 1, 16, 16, 64, torch.bfloat16, 1)]
+    cos, sin = ra.make_tables(16, 64, 10000.0)
+    with pytest.raises(ra.RAError) as e:
+        ra.attn_fwd_causal_rope(q, k, v, cos, sin, kv_offset=-1)
+    assert e.value.code == -1
+    short_c, short_s = cos[:8], sin[:8]
+    with pytest.raises(ra.RAError) as e:
+        ra.attn_fwd_causal_rope(q, k, v, short_c.contiguous(), short_s.contiguous())
+    assert e.value.code == -1
+    q96 = torch.zeros(1, 2, 16, 96, dtype=torch.bfloat16, device="cuda")
+    k96 = torch.zeros(1, 1, 16, 96, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ra.RAError) as e:
+        ra.attn_fwd_causal_rope(q96, k96, k96, apply_rope=False)
+    assert e.value.code == -2
+    assert ra.ra_get_device_status() == 0
