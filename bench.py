@@ -1,0 +1,360 @@
+"""Benchmark: fused RoPE causal attention TFLOP/s and rope_apply GB/s on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one fused RoPE causal attention forward over the long-context GQA
+workload (bf16, B=1, 32 q-heads / 8 kv-heads, 16384 new queries after a
+4096-row cached prefix, D=128, NeoX, base 5e5): the largest single-GPU
+configuration of the attention metric.  The same run also times the
+standalone rope_apply_qk on the continuous-batching workload (bf16, 65536
+tokens of 256 requests, 32 + 8 heads, D=128, in place) and reports its GB/s.
+
+Timing: W untimed warm-up steps, then K steps, each timed with CUDA events on
+the launching stream; L2 is flushed (a 256 MiB write) before every timed
+attention step; the rope working set (1.4 GB) is larger than L2.  A barrier
+and a device synchronize bracket the timed region; times are the max over
+ranks.  Under torchrun each rank runs an independent replica (the method has
+no exchange step), so scaling is weak.
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload (rows of the attention), same metric and unit.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+METRIC = "fused RoPE causal attn TFLOPS (% bf16 peak); rope_apply GB/s (% HBM), 1 GB300"
+ATTN = wl.LONG_GQA
+ROPE = wl.CB_ROPE
+ATTN_KERNEL_SRC = os.path.join(ROOT, "rope_causal_attention_gb300", "csrc", "attn_tc.cu")
+ROPE_KERNEL_SRC = os.path.join(ROOT, "rope_causal_attention_gb300", "csrc", "rope_kernels.cu")
+PROFILE_JSON = os.path.join(ROOT, "profiles", "counters.json")
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), float(m["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def src_hash(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def dram_traffic(kernel_key, src):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    try:
+        with open(PROFILE_JSON) as f:
+            d = json.load(f)[kernel_key]
+        if d.get("src_sha256_16") != src_hash(src):
+            return None
+        return int(d["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi during a region."""
+    Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = max(mx, float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[3:7]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_oracle_attention(sample_rows: int, seed: int = 0):
+    """Times the fp64 oracle on a seeded row sample of the attention workload.
+    Returns (TFLOP/s, seconds, threads, description)."""
+    import oracle
+    oracle.build()
+    q, k, v = ATTN.inputs()
+    qn, kn, vn = q.float().numpy(), k.float().numpy(), v.float().numpy()
+    rng = np.random.default_rng(seed)
+    n = ATTN.B * ATTN.Hq * ATTN.Sq
+    rows = np.sort(rng.choice(n, size=sample_rows, replace=False))
+    i = rows % ATTN.Sq
+    flops = float(4.0 * ATTN.D * np.minimum(ATTN.Sk, ATTN.kv_offset + i + 1).sum())
+    threads = oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.attention(qn, kn, vn, kv_offset=ATTN.kv_offset, base=ATTN.base, layout=ATTN.layout,
+                     rows=rows, nthreads=threads)
+    dt = time.perf_counter() - t0
+    desc = (f"{sample_rows} seeded random query rows of {n} (all heads), K rotation of all "
+            f"kv heads included; fp64 C oracle, {threads} threads")
+    return flops / dt / 1e12, dt, threads, desc
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return 0
+    sample = args.ref_rows
+    vals = []
+    for it in range(args.warmup + args.steps):
+        tf, dt, threads, desc = cpu_oracle_attention(sample, seed=it)
+        if it >= args.warmup:
+            vals.append((tf, dt))
+    value = statistics.mean(v[0] for v in vals)
+    ms = statistics.mean(v[1] for v in vals) * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": ATTN.name, "sample": f"{sample} rows per step"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, ws, rank, local):
+    import rope_causal_attention_gb300 as ra
+    from rope_causal_attention_gb300 import build as rbuild
+    if rank == 0 or not os.path.exists(ra.library_path()):
+        rbuild.build()
+    if ws > 1:
+        torch.distributed.barrier()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    hbm_peak, tf_peak, peak_kind = peaks()
+
+    # ---------------------------------------------------------------- inputs
+    q, k, v = ATTN.inputs()
+    qg, kg, vg = q.to(dev), k.to(dev), v.to(dev)
+    cos, sin = ra.make_tables(ATTN.Sk, ATTN.r, ATTN.base, device=dev)
+    o = torch.empty_like(qg)
+    lse = torch.empty(ATTN.B, ATTN.Hq, ATTN.Sq, dtype=torch.float32, device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    flops = ATTN.flops()
+
+    def attn_call():
+        ra.attn_fwd_causal_rope(qg, kg, vg, cos, sin, kv_offset=ATTN.kv_offset,
+                                layout=ATTN.layout, out=o, lse=lse)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        attn_call()
+    torch.cuda.synchronize()
+    if ra.ra_get_device_status() != 0:
+        raise RuntimeError("device status error during warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        for s in range(args.steps):
+            flush.zero_()
+            starts[s].record(stream)
+            attn_call()
+            ends[s].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    if ws > 1:
+        torch.distributed.barrier()
+    if ra.ra_get_device_status() != 0:
+        raise RuntimeError("device status error during timed steps")
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    ms = statistics.mean(step_ms)
+    ms_max = ms
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_max = float(t.item())
+    per_gpu_tflops = flops / (ms_max * 1e-3) / 1e12
+    value = per_gpu_tflops * ws
+
+    # ------------------------------------------------------ e2e (host buffers)
+    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lh = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    e2e_steps = max(1, min(args.steps, 5))
+    for it in range(1 + e2e_steps):
+        if it == 1:
+            torch.cuda.synchronize()
+            te = time.perf_counter()
+        qg.copy_(qh, non_blocking=True)
+        kg.copy_(kh, non_blocking=True)
+        vg.copy_(vh, non_blocking=True)
+        attn_call()
+        oh.copy_(o, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - te) / e2e_steps
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+    d2h = oh.numel() * oh.element_size() + lh.numel() * 4
+    del qh, kh, vh, oh, lh
+
+    # ------------------------------------------------------------ rope_apply
+    rq, rk = ROPE.inputs()
+    rpos = torch.from_numpy(ROPE.positions()).to(torch.int32).to(dev)
+    rqg, rkg = rq.to(dev), rk.to(dev)
+    rcos, rsin = ra.make_tables(ROPE.table_rows, ROPE.rot_dim, ROPE.base, device=dev)
+    for _ in range(max(3, args.warmup)):
+        ra.rope_apply_qk(rqg, rkg, rpos, rcos, rsin, layout=ROPE.layout)
+    torch.cuda.synchronize()
+    rs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    re_ = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for s in range(args.steps):
+        rs[s].record(stream)
+        ra.rope_apply_qk(rqg, rkg, rpos, rcos, rsin, layout=ROPE.layout)
+        re_[s].record(stream)
+    torch.cuda.synchronize()
+    if ra.ra_get_device_status() != 0:
+        raise RuntimeError("device status error in rope_apply")
+    rope_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(rs, re_))
+    rope_bytes = ROPE.algorithmic_bytes()
+    rope_gbs = rope_bytes / (rope_ms * 1e-3) / 1e9
+
+    # ---------------------------------------------------------- CPU baseline
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        tf, dt, threads, desc = cpu_oracle_attention(args.cpu_rows)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": desc + f"; {dt:.1f} s"}
+
+    if rank != 0:
+        return 0
+    traffic = dram_traffic("attn_tc_long_gqa", ATTN_KERNEL_SRC)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/k/v, workloads.LONG_GQA)",
+        "config": {"workload": ATTN.name, "B": ATTN.B, "Hq": ATTN.Hq, "Hkv": ATTN.Hkv,
+                   "Sq": ATTN.Sq, "Sk": ATTN.Sk, "D": ATTN.D, "kv_offset": ATTN.kv_offset,
+                   "layout": "neox", "base": ATTN.base, "flop_per_step": flops,
+                   "l2": "flushed before every timed step (256 MiB write)",
+                   "parallelism": f"replicas x{ws}"},
+        "roofline": {"bound": "tensor", "achieved": per_gpu_tflops, "peak": tf_peak,
+                     "unit": "TFLOP/s", "frac": per_gpu_tflops / tf_peak, "traffic": traffic,
+                     "peak_kind": f"{peak_kind} bf16 dense (burst)"},
+        "rope_apply": {"workload": ROPE.name, "value": rope_gbs, "unit": "GB/s",
+                       "ms": rope_ms, "algorithmic_bytes": rope_bytes,
+                       "roofline": {"bound": "hbm", "achieved": rope_gbs, "peak": hbm_peak,
+                                    "unit": "GB/s", "frac": rope_gbs / hbm_peak,
+                                    "traffic": dram_traffic("rope_apply_cb", ROPE_KERNEL_SRC),
+                                    "peak_kind": f"{peak_kind} HBM copy"},
+                       "l2": "working set 1.4 GB > L2"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": flops / e2e_s / 1e12 * ws, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": wall,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-rows", type=int, default=4096)
+    ap.add_argument("--ref-rows", type=int, default=2048)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    ws, rank, local = dist_env()
+    if ws > 1:
+        backend = "nccl" if torch.cuda.is_available() and args.impl == "ours" else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        torch.distributed.init_process_group(backend)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, ws, rank)
+        return run_ours(args, ws, rank, local)
+    finally:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())
