@@ -1,7 +1,9 @@
 """GPU parity: attn_fwd_causal_rope against the fp64 oracle.
 
 Tolerances (max absolute error against the fp64 result): O <= 2e-2 for
-bf16/fp16 inputs and <= 1e-4 for fp32 inputs; LSE <= 1e-3 for every dtype.
+bf16/fp16 inputs and <= 1e-4 for fp32 inputs; LSE <= 1e-3 for every dtype at
+the default scale 1/sqrt(D) (for bf16/fp16 with a larger custom scale the LSE
+bound grows by scale * sqrt(D), as the score error does).
 Inputs are the seeded tensors of ``workloads``.
 """
 import numpy as np
@@ -61,6 +63,10 @@ def run_case(ra, orc, dt, B, Hq, Hkv, Sq, Sk, D, off, layout=NEOX, rot_dim=None,
     eo = np.abs(og - o_ref).max()
     el = np.abs(lg - lse_ref).max()
     to, tl = TOL[dt]
+    if scale is not None and dt != torch.float32:
+        # the fp16 rounding error of every score grows linearly with the scale:
+        # the stated LSE bound applies at 1/sqrt(D) and scales with it
+        tl *= max(1.0, scale * np.sqrt(D))
     assert np.isfinite(og).all() and np.isfinite(lg).all()
     assert eo <= to and el <= tl, f"O err {eo:.3g} (tol {to}), LSE err {el:.3g} (tol {tl})"
     return eo, el
