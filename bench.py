@@ -96,7 +96,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -138,13 +138,18 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+_CPU_INPUTS = {}
+
+
 def cpu_oracle_attention(sample_rows: int, seed: int = 0):
     """Times the fp64 oracle on a seeded row sample of the attention workload.
     Returns (TFLOP/s, seconds, threads, description)."""
     import oracle
     oracle.build()
-    q, k, v = ATTN.inputs()
-    qn, kn, vn = q.float().numpy(), k.float().numpy(), v.float().numpy()
+    if "attn" not in _CPU_INPUTS:
+        q, k, v = ATTN.inputs()
+        _CPU_INPUTS["attn"] = (q.float().numpy(), k.float().numpy(), v.float().numpy())
+    qn, kn, vn = _CPU_INPUTS["attn"]
     rng = np.random.default_rng(seed)
     n = ATTN.B * ATTN.Hq * ATTN.Sq
     rows = np.sort(rng.choice(n, size=sample_rows, replace=False))
@@ -186,6 +191,110 @@ def run_reference(args, ws, rank):
     return 0
 
 
+def attn_workload(args):
+    if args.attn_sq:
+        import dataclasses
+        return dataclasses.replace(ATTN, Sq=args.attn_sq, Sk=args.attn_sq + ATTN.kv_offset,
+                                   name=f"{ATTN.name}__Sq{args.attn_sq}")
+    return ATTN
+
+
+def time_attention(ra, W, args, dev, stream, ws, local, host_e2e=True):
+    """Times W warm-up + K steps of the fused attention; returns a dict."""
+    q, k, v = W.inputs()
+    qg, kg, vg = q.to(dev), k.to(dev), v.to(dev)
+    cos, sin = ra.make_tables(max(W.Sk, W.kv_offset + W.Sq), W.r, W.base, device=dev)
+    o = torch.empty_like(qg)
+    lse = torch.empty(W.B, W.Hq, W.Sq, dtype=torch.float32, device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def call():
+        ra.attn_fwd_causal_rope(qg, kg, vg, cos, sin, kv_offset=W.kv_offset, layout=W.layout,
+                                out=o, lse=lse)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    if ra.ra_get_device_status() != 0:
+        raise RuntimeError("device status error during warm-up")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        time.sleep(0.05)  # let the sampler start before the timed region
+        t0 = time.perf_counter()
+        for s in range(args.steps):
+            flush.zero_()
+            starts[s].record(stream)
+            call()
+            ends[s].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    if ws > 1:
+        torch.distributed.barrier()
+    if ra.ra_get_device_status() != 0:
+        raise RuntimeError("device status error during timed steps")
+    ms = statistics.mean(a.elapsed_time(b) for a, b in zip(starts, ends))
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    out = {"ms": ms, "wall": wall, "clocks": clk.summary(), "flops": W.flops()}
+    if host_e2e:
+        # the same call through host buffers: H2D of q, k, v and D2H of O, LSE each step
+        qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+        oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        lh = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+        n = max(1, min(args.steps, 5))
+        for it in range(1 + n):
+            if it == 1:
+                torch.cuda.synchronize()
+                te = time.perf_counter()
+            qg.copy_(qh, non_blocking=True)
+            kg.copy_(kh, non_blocking=True)
+            vg.copy_(vh, non_blocking=True)
+            call()
+            oh.copy_(o, non_blocking=True)
+            lh.copy_(lse, non_blocking=True)
+        torch.cuda.synchronize()
+        out["e2e_s"] = (time.perf_counter() - te) / n
+        out["h2d"] = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+        out["d2h"] = oh.numel() * oh.element_size() + lh.numel() * 4
+    return out
+
+
+def time_rope(ra, args, dev, stream):
+    """Times the in-place rope_apply_qk over the continuous-batching batch
+    (its 1.4 GB working set exceeds L2, so no flush is needed)."""
+    rq, rk = ROPE.inputs()
+    pos = ROPE.positions()
+    T = ROPE.T
+    if args.rope_tokens:
+        T = args.rope_tokens
+        rq, rk, pos = rq[:T], rk[:T], pos[:T]
+    rpos = torch.from_numpy(pos).to(torch.int32).to(dev)
+    rqg, rkg = rq.to(dev), rk.to(dev)
+    rcos, rsin = ra.make_tables(ROPE.table_rows, ROPE.rot_dim, ROPE.base, device=dev)
+    for _ in range(args.warmup):
+        ra.rope_apply_qk(rqg, rkg, rpos, rcos, rsin, layout=ROPE.layout)
+    torch.cuda.synchronize()
+    rs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    re_ = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for s in range(args.steps):
+        rs[s].record(stream)
+        ra.rope_apply_qk(rqg, rkg, rpos, rcos, rsin, layout=ROPE.layout)
+        re_[s].record(stream)
+    torch.cuda.synchronize()
+    if ra.ra_get_device_status() != 0:
+        raise RuntimeError("device status error in rope_apply")
+    ms = statistics.mean(a.elapsed_time(b) for a, b in zip(rs, re_))
+    nbytes = ROPE.algorithmic_bytes() * T // ROPE.T
+    return {"ms": ms, "bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9, "T": T}
+
+
 def run_ours(args, ws, rank, local):
     import rope_causal_attention_gb300 as ra
     from rope_causal_attention_gb300 import build as rbuild
@@ -198,132 +307,58 @@ def run_ours(args, ws, rank, local):
     stream = torch.cuda.current_stream(dev)
     hbm_peak, tf_peak, peak_kind = peaks()
 
-    # ---------------------------------------------------------------- inputs
-    q, k, v = ATTN.inputs()
-    qg, kg, vg = q.to(dev), k.to(dev), v.to(dev)
-    cos, sin = ra.make_tables(ATTN.Sk, ATTN.r, ATTN.base, device=dev)
-    o = torch.empty_like(qg)
-    lse = torch.empty(ATTN.B, ATTN.Hq, ATTN.Sq, dtype=torch.float32, device=dev)
-    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    flops = ATTN.flops()
+    if args.only == "rope":
+        r = time_rope(ra, args, dev, stream)
+        if rank == 0:
+            print(json.dumps({"only": "rope", "workload": ROPE.name, "tokens": r["T"],
+                              "ms": r["ms"], "GB/s": r["gbs"], "frac": r["gbs"] / hbm_peak}))
+        return 0
+    W = attn_workload(args)
+    a = time_attention(ra, W, args, dev, stream, ws, local, host_e2e=args.only == "all")
+    per_gpu_tflops = a["flops"] / (a["ms"] * 1e-3) / 1e12
+    if args.only == "attn":
+        if rank == 0:
+            print(json.dumps({"only": "attn", "workload": W.name, "ms": a["ms"],
+                              "TFLOP/s": per_gpu_tflops, "frac": per_gpu_tflops / tf_peak,
+                              "clocks": a["clocks"]}))
+        return 0
+    r = time_rope(ra, args, dev, stream)
 
-    def attn_call():
-        ra.attn_fwd_causal_rope(qg, kg, vg, cos, sin, kv_offset=ATTN.kv_offset,
-                                layout=ATTN.layout, out=o, lse=lse)
-
-    for _ in range(args.warmup):
-        flush.zero_()
-        attn_call()
-    torch.cuda.synchronize()
-    if ra.ra_get_device_status() != 0:
-        raise RuntimeError("device status error during warm-up")
-
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    if ws > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        t0 = time.perf_counter()
-        for s in range(args.steps):
-            flush.zero_()
-            starts[s].record(stream)
-            attn_call()
-            ends[s].record(stream)
-        torch.cuda.synchronize()
-        wall = time.perf_counter() - t0
-    if ws > 1:
-        torch.distributed.barrier()
-    if ra.ra_get_device_status() != 0:
-        raise RuntimeError("device status error during timed steps")
-    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
-    ms = statistics.mean(step_ms)
-    ms_max = ms
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_max = float(t.item())
-    per_gpu_tflops = flops / (ms_max * 1e-3) / 1e12
-    value = per_gpu_tflops * ws
-
-    # ------------------------------------------------------ e2e (host buffers)
-    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
-    oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    lh = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
-    e2e_steps = max(1, min(args.steps, 5))
-    for it in range(1 + e2e_steps):
-        if it == 1:
-            torch.cuda.synchronize()
-            te = time.perf_counter()
-        qg.copy_(qh, non_blocking=True)
-        kg.copy_(kh, non_blocking=True)
-        vg.copy_(vh, non_blocking=True)
-        attn_call()
-        oh.copy_(o, non_blocking=True)
-        lh.copy_(lse, non_blocking=True)
-    torch.cuda.synchronize()
-    e2e_s = (time.perf_counter() - te) / e2e_steps
-    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
-    d2h = oh.numel() * oh.element_size() + lh.numel() * 4
-    del qh, kh, vh, oh, lh
-
-    # ------------------------------------------------------------ rope_apply
-    rq, rk = ROPE.inputs()
-    rpos = torch.from_numpy(ROPE.positions()).to(torch.int32).to(dev)
-    rqg, rkg = rq.to(dev), rk.to(dev)
-    rcos, rsin = ra.make_tables(ROPE.table_rows, ROPE.rot_dim, ROPE.base, device=dev)
-    for _ in range(max(3, args.warmup)):
-        ra.rope_apply_qk(rqg, rkg, rpos, rcos, rsin, layout=ROPE.layout)
-    torch.cuda.synchronize()
-    rs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    re_ = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    for s in range(args.steps):
-        rs[s].record(stream)
-        ra.rope_apply_qk(rqg, rkg, rpos, rcos, rsin, layout=ROPE.layout)
-        re_[s].record(stream)
-    torch.cuda.synchronize()
-    if ra.ra_get_device_status() != 0:
-        raise RuntimeError("device status error in rope_apply")
-    rope_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(rs, re_))
-    rope_bytes = ROPE.algorithmic_bytes()
-    rope_gbs = rope_bytes / (rope_ms * 1e-3) / 1e9
-
-    # ---------------------------------------------------------- CPU baseline
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         tf, dt, threads, desc = cpu_oracle_attention(args.cpu_rows)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": desc + f"; {dt:.1f} s"}
-
     if rank != 0:
         return 0
-    traffic = dram_traffic("attn_tc_long_gqa", ATTN_KERNEL_SRC)
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "metric": METRIC, "value": per_gpu_tflops * ws, "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": a["ms"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) q/k/v, workloads.LONG_GQA)",
-        "config": {"workload": ATTN.name, "B": ATTN.B, "Hq": ATTN.Hq, "Hkv": ATTN.Hkv,
-                   "Sq": ATTN.Sq, "Sk": ATTN.Sk, "D": ATTN.D, "kv_offset": ATTN.kv_offset,
-                   "layout": "neox", "base": ATTN.base, "flop_per_step": flops,
+        "config": {"workload": W.name, "B": W.B, "Hq": W.Hq, "Hkv": W.Hkv, "Sq": W.Sq,
+                   "Sk": W.Sk, "D": W.D, "kv_offset": W.kv_offset, "layout": "neox",
+                   "base": W.base, "flop_per_step": a["flops"],
                    "l2": "flushed before every timed step (256 MiB write)",
                    "parallelism": f"replicas x{ws}"},
         "roofline": {"bound": "tensor", "achieved": per_gpu_tflops, "peak": tf_peak,
-                     "unit": "TFLOP/s", "frac": per_gpu_tflops / tf_peak, "traffic": traffic,
+                     "unit": "TFLOP/s", "frac": per_gpu_tflops / tf_peak,
+                     "traffic": dram_traffic("attn_tc_long_gqa", ATTN_KERNEL_SRC),
                      "peak_kind": f"{peak_kind} bf16 dense (burst)"},
-        "rope_apply": {"workload": ROPE.name, "value": rope_gbs, "unit": "GB/s",
-                       "ms": rope_ms, "algorithmic_bytes": rope_bytes,
-                       "roofline": {"bound": "hbm", "achieved": rope_gbs, "peak": hbm_peak,
-                                    "unit": "GB/s", "frac": rope_gbs / hbm_peak,
+        "rope_apply": {"workload": ROPE.name, "value": r["gbs"], "unit": "GB/s", "ms": r["ms"],
+                       "algorithmic_bytes": r["bytes"],
+                       "roofline": {"bound": "hbm", "achieved": r["gbs"], "peak": hbm_peak,
+                                    "unit": "GB/s", "frac": r["gbs"] / hbm_peak,
                                     "traffic": dram_traffic("rope_apply_cb", ROPE_KERNEL_SRC),
                                     "peak_kind": f"{peak_kind} HBM copy"},
                        "l2": "working set 1.4 GB > L2"},
         "cpu_baseline": cpu,
-        "e2e": {"value": flops / e2e_s / 1e12 * ws, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
+        "e2e": {"value": a["flops"] / a["e2e_s"] / 1e12 * ws, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": a["h2d"], "d2h_bytes_per_step": a["d2h"],
+                "ms_per_step": a["e2e_s"] * 1e3},
         "gpu_launches": args.steps,
-        "clocks": clk.summary(),
-        "wall_s_timed_region": wall,
+        "clocks": a["clocks"],
+        "wall_s_timed_region": a["wall"],
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -332,12 +367,19 @@ def run_ours(args, ws, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-rows", type=int, default=4096)
     ap.add_argument("--ref-rows", type=int, default=2048)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["all", "attn", "rope"], default="all",
+                    help="profiling aid: time one kernel only (no e2e, no CPU baseline)")
+    ap.add_argument("--attn-sq", type=int, default=0,
+                    help="profiling aid: shrink the attention workload to this many new "
+                         "queries (the 4096-row cached prefix is kept)")
+    ap.add_argument("--rope-tokens", type=int, default=0,
+                    help="profiling aid: rotate only the first N tokens of the batch")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -13,7 +13,8 @@
 // ------------
 // One CTA owns two 128-row query "slots" that share every K/V tile: two
 // q-heads of one kv group at the same rows (grouped-query attention), or two
-// consecutive 128-row tiles of one head.  Warp roles (448 threads):
+// consecutive 128-row tiles of one head.  Warp roles (512 threads, four
+// warpgroups whose register shares are re-balanced with setmaxnreg):
 //   warps 0-3   softmax for slot 0 (thread = query row = TMEM lane)
 //   warps 4-7   softmax for slot 1
 //   warps 8-11  rotation: Q tiles once, then each K tile as it is staged:
@@ -21,6 +22,7 @@
 //               -> fp16 operand in 128B-swizzled shared memory
 //   warp 12     TMA producer for V tiles (raw, never rotated)
 //   warp 13     tcgen05 MMA issuer; owns the tensor-memory allocation
+//   warps 14-15 idle (complete the fourth warpgroup)
 // Tensor memory (512 columns): S0 | S1 | O0 | O1.  P is written as 16-bit
 // pairs over the first 64 columns of its S block and fed to the PV product
 // straight from tensor memory.  The issue order S0(n+1) after PV0(n) and
@@ -52,7 +54,7 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 448;
+constexpr int kThreads = 512;  // four full warpgroups
 constexpr int kWarpRot = 8;
 constexpr int kWarpTma = 12;
 constexpr int kWarpMma = 13;
@@ -94,6 +96,7 @@ struct TcParams {
   int Hq, G, n_units, units_per_b, n_qt, pack_heads;
   int apply_rope, rot_dim, layout;
   const float *cos_t, *sin_t;
+  int64_t table_rows;
   float scale_log2;
   int vperm[3];  // tensor-map dims 1..3 -> logical coordinate (0 key row, 1 kv head, 2 batch)
   int *status;
@@ -243,6 +246,193 @@ __device__ __forceinline__ void rotate_row(const TIn *src, bool valid, int64_t p
   }
 }
 
+// ------------------------------------------------ full-rotation tile path
+// Used when rot_dim == D.  Thread t of the rotation warpgroup owns NP pairs
+// (chunk c = t % CH of a row) over RPG consecutive rows starting at row
+// g * RPG (g = t / CH), so the CH lanes of a row read its 16-byte chunks
+// contiguously.  cos/sin come from the table row of the group's first
+// position; each following row advances them by one step of angle addition
+// with (cos theta_i, sin theta_i) from table row 1, in fp32:
+//   cos((p+1)theta) = cos(p theta) cos theta - sin(p theta) sin theta,
+//   sin((p+1)theta) = sin(p theta) cos theta + cos(p theta) sin theta.
+// Arithmetic runs on packed fp32 pairs (two pairs per instruction).  For
+// GPT-J the even/odd members of the pairs in a 16-byte chunk play the roles
+// of the NeoX low/high halves, so both layouts share one code path.
+template <int D, int LAYOUT>
+struct FullRot {
+  static constexpr int NP = (LAYOUT == RA_NEOX) ? 8 : 4;          // pairs per thread per row
+  static constexpr int CH = (LAYOUT == RA_NEOX) ? D / 16 : D / 8;  // threads per row
+  static constexpr int RPG = CH;                                   // rows per thread
+  static constexpr int LD = (LAYOUT == RA_NEOX) ? 2 : 1;           // 16-byte loads per row
+  static constexpr int NG = NP / 2;                                // float2 groups per row
+};
+
+template <typename TIn> __device__ __forceinline__ float2 unpack2(uint32_t w);
+template <> __device__ __forceinline__ float2 unpack2<__nv_bfloat16>(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+template <> __device__ __forceinline__ float2 unpack2<__half>(uint32_t w) {
+  return __half22float2(*reinterpret_cast<const __half2 *>(&w));
+}
+__device__ __forceinline__ uint32_t w_of(const uint4 &u, int k) {
+  return k == 0 ? u.x : (k == 1 ? u.y : (k == 2 ? u.z : u.w));
+}
+
+template <int D, typename TIn, int LAYOUT>
+__device__ __forceinline__ void full_rot_load(
+    const TIn *rows, int64_t row_stride, int64_t nvalid, int t,
+    uint4 (&raw)[FullRot<D, LAYOUT>::RPG][FullRot<D, LAYOUT>::LD]) {
+  using F = FullRot<D, LAYOUT>;
+  const int c = t % F::CH, r0 = (t / F::CH) * F::RPG;
+#pragma unroll
+  for (int r = 0; r < F::RPG; ++r) {
+    const bool ok = r0 + r < nvalid;
+    const uint4 *src = reinterpret_cast<const uint4 *>(rows + (ok ? (r0 + r) : 0) * row_stride);
+#pragma unroll
+    for (int l = 0; l < F::LD; ++l)
+      raw[r][l] = ok ? __ldg(src + ((LAYOUT == RA_NEOX) ? c + l * (D / 16) : c))
+                     : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// cos/sin of this thread's pairs at `pos` (table row), as float2 groups.
+template <int D, int LAYOUT>
+__device__ __forceinline__ void full_rot_table(const TcParams &p, int64_t pos, int t,
+                                               float2 (&cv)[FullRot<D, LAYOUT>::NG],
+                                               float2 (&sv)[FullRot<D, LAYOUT>::NG]) {
+  using F = FullRot<D, LAYOUT>;
+  const int pair0 = (t % F::CH) * F::NP;
+  const float4 *c4 = reinterpret_cast<const float4 *>(p.cos_t + pos * (D / 2) + pair0);
+  const float4 *s4 = reinterpret_cast<const float4 *>(p.sin_t + pos * (D / 2) + pair0);
+#pragma unroll
+  for (int q = 0; q < F::NP / 4; ++q) {
+    const float4 a = __ldg(c4 + q), b = __ldg(s4 + q);
+    cv[2 * q] = make_float2(a.x, a.y);
+    cv[2 * q + 1] = make_float2(a.z, a.w);
+    sv[2 * q] = make_float2(b.x, b.y);
+    sv[2 * q + 1] = make_float2(b.z, b.w);
+  }
+}
+
+template <int D, typename TIn, int LAYOUT>
+__device__ __forceinline__ void full_rot_store(
+    const uint4 (&raw)[FullRot<D, LAYOUT>::RPG][FullRot<D, LAYOUT>::LD],
+    float2 (&cb)[FullRot<D, LAYOUT>::NG], float2 (&sb)[FullRot<D, LAYOUT>::NG],
+    const float2 (&cst)[FullRot<D, LAYOUT>::NG], const float2 (&sst)[FullRot<D, LAYOUT>::NG],
+    uint8_t *tile, int t) {
+  using F = FullRot<D, LAYOUT>;
+  const int c = t % F::CH, r0 = (t / F::CH) * F::RPG;
+#pragma unroll
+  for (int r = 0; r < F::RPG; ++r) {
+    const int row = r0 + r;
+    uint32_t olo[4], ohi[4];
+#pragma unroll
+    for (int j = 0; j < F::NG; ++j) {
+      float2 L, H;
+      if (LAYOUT == RA_NEOX) {
+        L = unpack2<TIn>(w_of(raw[r][0], j));
+        H = unpack2<TIn>(w_of(raw[r][1], j));
+      } else {  // words 2j and 2j+1 hold pairs (a, b); evens -> L, odds -> H
+        const float2 u = unpack2<TIn>(w_of(raw[r][0], 2 * j));
+        const float2 v = unpack2<TIn>(w_of(raw[r][0], 2 * j + 1));
+        L = make_float2(u.x, v.x);
+        H = make_float2(u.y, v.y);
+      }
+      const float2 lc = __fmul2_rn(L, cb[j]);
+      const float2 hc = __fmul2_rn(H, cb[j]);
+      const float2 a = __ffma2_rn(make_float2(-H.x, -H.y), sb[j], lc);  // lo*c - hi*s
+      const float2 b = __ffma2_rn(L, sb[j], hc);                         // hi*c + lo*s
+      if (LAYOUT == RA_NEOX) {
+        olo[j] = f16x2(a.x, a.y);
+        ohi[j] = f16x2(b.x, b.y);
+      } else {
+        olo[2 * j] = f16x2(a.x, b.x);
+        olo[2 * j + 1] = f16x2(a.y, b.y);
+      }
+    }
+    const int sw = row & 7;
+    if (LAYOUT == RA_NEOX) {
+      *reinterpret_cast<uint4 *>(tile + (c >> 3) * 16384 + row * 128 + (((c & 7) ^ sw) << 4)) =
+          make_uint4(olo[0], olo[1], olo[2], olo[3]);
+      const int ch = c + D / 16;
+      *reinterpret_cast<uint4 *>(tile + (ch >> 3) * 16384 + row * 128 + (((ch & 7) ^ sw) << 4)) =
+          make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
+    } else {
+      *reinterpret_cast<uint4 *>(tile + (c >> 3) * 16384 + row * 128 + (((c & 7) ^ sw) << 4)) =
+          make_uint4(olo[0], olo[1], olo[2], olo[3]);
+    }
+    if (r + 1 < F::RPG) {
+#pragma unroll
+      for (int j = 0; j < F::NG; ++j) {
+        const float2 cn = __ffma2_rn(cb[j], cst[j], __fmul2_rn(make_float2(-sb[j].x, -sb[j].y), sst[j]));
+        sb[j] = __ffma2_rn(sb[j], cst[j], __fmul2_rn(cb[j], sst[j]));
+        cb[j] = cn;
+      }
+    }
+  }
+}
+
+// Whole-tile rotation without prefetch (Q tiles, once per CTA).
+template <int D, typename TIn, int LAYOUT>
+__device__ __forceinline__ void rotate_tile_full(const TIn *rows, int64_t row_stride,
+                                                 int64_t nvalid, int64_t pos0, uint8_t *tile,
+                                                 int t, const TcParams &p) {
+  using F = FullRot<D, LAYOUT>;
+  uint4 raw[F::RPG][F::LD];
+  float2 cb[F::NG], sb[F::NG], cst[F::NG], sst[F::NG];
+  const int64_t r0 = (t / F::CH) * F::RPG;
+  full_rot_load<D, TIn, LAYOUT>(rows, row_stride, nvalid, t, raw);
+  full_rot_table<D, LAYOUT>(p, r0 < nvalid ? pos0 + r0 : 0, t, cb, sb);
+  full_rot_table<D, LAYOUT>(p, p.table_rows > 1 ? 1 : 0, t, cst, sst);
+  full_rot_store<D, TIn, LAYOUT>(raw, cb, sb, cst, sst, tile, t);
+}
+
+// K tiles of the whole key loop: the next tile's rows are loaded into
+// registers before waiting for its shared-memory stage to be released.
+template <int D, typename TIn, int LAYOUT, int NS>
+__device__ __forceinline__ void rotate_k_loop(const TIn *kbase, const TcParams &p, int N, int t,
+                                              uint8_t *k_tiles, uint32_t kfull0,
+                                              uint32_t kempty0, const Ctl &ctl) {
+  using F = FullRot<D, LAYOUT>;
+  constexpr int TILE = 128 * D * 2;
+  uint4 raw[F::RPG][F::LD];
+  float2 cb[F::NG], sb[F::NG], cst[F::NG], sst[F::NG];
+  const int64_t r0 = (t / F::CH) * F::RPG;
+  full_rot_table<D, LAYOUT>(p, p.table_rows > 1 ? 1 : 0, t, cst, sst);
+  if (N > 0) full_rot_load<D, TIn, LAYOUT>(kbase, p.sk2, p.Sk, t, raw);
+  for (int n = 0; n < N; ++n) {
+    const int st = n % NS;
+    const int64_t j0 = (int64_t)n * 128;
+    full_rot_table<D, LAYOUT>(p, r0 < p.Sk - j0 ? j0 + r0 : 0, t, cb, sb);
+    if (n >= NS && !wait_bar(kempty0 + 8u * st, (uint32_t)((n / NS - 1) & 1), ctl)) break;
+    full_rot_store<D, TIn, LAYOUT>(raw, cb, sb, cst, sst, k_tiles + st * TILE, t);
+    fence_proxy_async_smem();
+    mbar_arrive(kfull0 + 8u * st);
+    if (n + 1 < N) {
+      const int64_t j1 = j0 + 128;
+      full_rot_load<D, TIn, LAYOUT>(kbase + j1 * p.sk2, p.sk2, p.Sk - j1, t, raw);
+    }
+  }
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Register shares after re-allocation (per thread).  The four warpgroups sum
+// to 512, i.e. exactly the 512 threads x 128 registers the block launches
+// with; the host refuses to launch a build that did not allocate 128.
+constexpr uint32_t kRegSoftmax = 160;
+constexpr uint32_t kRegRotate = 144;
+constexpr uint32_t kRegCtrl = 48;
+static_assert(2 * kRegSoftmax + kRegRotate + kRegCtrl == 4 * 128, "register split");
+
+// Lazy rescaling: the exponent reference moves only when the row max grows by
+// more than 2^kTau, so P <= 2^kTau and O/l are rescaled rarely.
+constexpr float kTau = 8.0f;
+
 template <int D, typename TIn>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, const TcParams p) {
@@ -264,28 +454,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int qt = p.n_qt - 1 - bid / p.n_units;
   const int unit = bid % p.n_units;
   const int b = unit / p.units_per_b, hu = unit % p.units_per_b;
-  int h[2];
-  int64_t m0[2];
-  if (p.pack_heads) {
-    h[0] = 2 * hu;
-    h[1] = 2 * hu + 1;
-    m0[0] = m0[1] = (int64_t)qt * 128;
-  } else {
-    h[0] = h[1] = hu;
-    m0[0] = (int64_t)qt * 256;
-    m0[1] = m0[0] + 128;
-  }
-  const int hk = h[0] / p.G;
+  const int h0 = p.pack_heads ? 2 * hu : hu;
+  const int h1 = p.pack_heads ? 2 * hu + 1 : hu;
+  const int64_t m00 = p.pack_heads ? (int64_t)qt * 128 : (int64_t)qt * 256;
+  const int64_t m01 = p.pack_heads ? m00 : m00 + 128;
+  const int hk = h0 / p.G;
   const int nkt = (int)((p.Sk + 127) / 128);
-  bool act[2];
-  int nend[2];
-#pragma unroll
-  for (int s = 0; s < 2; ++s) {
-    act[s] = m0[s] < p.Sq;
-    const int64_t last = min(m0[s] + 127, p.Sq - 1);
-    nend[s] = act[s] ? (int)min((int64_t)nkt, (last + p.kv_off) / 128 + 1) : 0;
-  }
-  const int N = max(nend[0], nend[1]);
+  const bool act0 = m00 < p.Sq, act1 = m01 < p.Sq;
+  const int nend0 = act0 ? (int)min((int64_t)nkt, (min(m00 + 127, p.Sq - 1) + p.kv_off) / 128 + 1) : 0;
+  const int nend1 = act1 ? (int)min((int64_t)nkt, (min(m01 + 127, p.Sq - 1) + p.kv_off) / 128 + 1) : 0;
+  const int N = max(nend0, nend1);
 
   // ---- set-up: barriers, tensor memory
   if (threadIdx.x == 0) {
@@ -319,71 +497,84 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 8) {
     // ================================================================ softmax
+    setmaxnreg_inc<kRegSoftmax>();
     const int slot = warp >> 2;
     const int wq = warp & 3;
     const int t = wq * 32 + lane;
     const uint32_t lane_bits = (uint32_t)(wq * 32) << 16;
     const uint32_t tS = tmem + lane_bits + C::s_col(slot);
     const uint32_t tO = tmem + lane_bits + C::o_col(slot);
-    if (act[slot]) {
-      const int64_t i = m0[slot] + t;
+    const bool act = slot ? act1 : act0;
+    const int nend = slot ? nend1 : nend0;
+    const int64_t m0 = slot ? m01 : m00;
+    const int hq = slot ? h1 : h0;
+    if (act) {
+      const int64_t i = m0 + t;
       const int64_t qpos = p.kv_off + i;
       const float sl2 = p.scale_log2;
-      float m = -INFINITY, l = 0.f;
+      float m_used = -INFINITY, l = 0.f;
       bool ok = true;
-      for (int n = 0; n < nend[slot]; ++n) {
+      for (int n = 0; n < nend; ++n) {
         if (!wait_bar(bar(C::B_SFULL + slot), (uint32_t)(n & 1), ctl)) { ok = false; break; }
         tc_fence_after();
         const int64_t j0 = (int64_t)n * 128;
-        const bool need_mask = (j0 + 127 > m0[slot] + p.kv_off) || (j0 + 127 >= p.Sk);
-        const int64_t jlim = min(qpos, p.Sk - 1);  // last admissible key of this row
-        float mx = -INFINITY;
+        uint32_t r[128];
+        tmem_ld128(tS, r);
+        if ((j0 + 127 > m0 + p.kv_off) || (j0 + 127 >= p.Sk)) {
+          // straddling tile: last admissible column of this row (-1: none)
+          const int lim = (int)max(min(min(qpos, p.Sk - 1) - j0, (int64_t)127), (int64_t)-1);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tS + 32 * c, r);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            float x = __uint_as_float(r[e]);
-            if (need_mask && j0 + 32 * c + e > jlim) x = -INFINITY;
-            mx = fmaxf(mx, x);
-          }
+          for (int e = 0; e < 128; ++e)
+            if (e > lim) r[e] = __float_as_uint(-INFINITY);
         }
-        const float m_new = fmaxf(m, mx * sl2);
-        const float alpha = ex2(m - m_new);
-        float rs = 0.f;
+        float mx = max3(__uint_as_float(r[0]), __uint_as_float(r[1]), __uint_as_float(r[2]));
+#pragma unroll
+        for (int e = 3; e < 127; e += 2)
+          mx = max3(mx, __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
+        mx = fmaxf(mx, __uint_as_float(r[127]));
+        const float m_tile = mx * sl2;
+        float alpha = 1.f;
+        const bool resc = m_tile > m_used + kTau;
+        if (resc) {
+          alpha = ex2(m_used - m_tile);
+          m_used = m_tile;
+        }
+        const float2 sl2v = make_float2(sl2, sl2);
+        const float2 negm = make_float2(-m_used, -m_used);
+        float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          uint32_t r[32], pk[16];
-          tmem_ld32(tS + 32 * c, r);
+          uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
-            float x0 = __uint_as_float(r[e]), x1 = __uint_as_float(r[e + 1]);
-            if (need_mask) {
-              if (j0 + 32 * c + e > jlim) x0 = -INFINITY;
-              if (j0 + 32 * c + e + 1 > jlim) x1 = -INFINITY;
-            }
-            const float p0 = ex2(fmaf(x0, sl2, -m_new));
-            const float p1 = ex2(fmaf(x1, sl2, -m_new));
-            rs += p0 + p1;
+            const float2 x = __ffma2_rn(
+                make_float2(__uint_as_float(r[32 * c + e]), __uint_as_float(r[32 * c + e + 1])),
+                sl2v, negm);
+            const float p0 = ex2(x.x), p1 = ex2(x.y);
+            acc = __fadd2_rn(acc, make_float2(p0, p1));
             pk[e >> 1] = In16<TIn>::pack2(p0, p1);
           }
           tmem_st16(tS + 16 * c, pk);  // P over the first 64 columns of S
         }
         tmem_st_wait();
-        l = l * alpha + rs;
-        if (n > 0 && __any_sync(0xffffffffu, alpha < 1.f)) {
+        l = l * alpha + (acc.x + acc.y);
+        if (n > 0 && __any_sync(0xffffffffu, resc)) {
+          const float2 av = make_float2(alpha, alpha);
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld32(tO + 32 * c, r);
+            uint32_t o[32];
+            tmem_ld32(tO + 32 * c, o);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-            tmem_st32(tO + 32 * c, r);
+            for (int e = 0; e < 32; e += 2) {
+              const float2 y = __fmul2_rn(
+                  make_float2(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), av);
+              o[e] = __float_as_uint(y.x);
+              o[e + 1] = __float_as_uint(y.y);
+            }
+            tmem_st32(tO + 32 * c, o);
           }
           tmem_st_wait();
         }
-        m = m_new;
         tc_fence_before();
         mbar_arrive(bar(C::B_PFULL + slot));
       }
@@ -392,145 +583,174 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const float inv_l = 1.f / l;
         const bool row_ok = i < p.Sq;
-        TIn *dst = static_cast<TIn *>(p.o) + b * p.so0 + h[slot] * p.so1 + i * p.so2;
+        TIn *dst = static_cast<TIn *>(p.o) + b * p.so0 + hq * p.so1 + i * p.so2;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tO + 32 * c, r);
+          uint32_t o[32];
+          tmem_ld32(tO + 32 * c, o);
           if (row_ok) {
             uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * c);
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
               uint4 u;
-              u.x = In16<TIn>::pack2(__uint_as_float(r[8 * g + 0]) * inv_l,
-                                     __uint_as_float(r[8 * g + 1]) * inv_l);
-              u.y = In16<TIn>::pack2(__uint_as_float(r[8 * g + 2]) * inv_l,
-                                     __uint_as_float(r[8 * g + 3]) * inv_l);
-              u.z = In16<TIn>::pack2(__uint_as_float(r[8 * g + 4]) * inv_l,
-                                     __uint_as_float(r[8 * g + 5]) * inv_l);
-              u.w = In16<TIn>::pack2(__uint_as_float(r[8 * g + 6]) * inv_l,
-                                     __uint_as_float(r[8 * g + 7]) * inv_l);
+              u.x = In16<TIn>::pack2(__uint_as_float(o[8 * g + 0]) * inv_l,
+                                     __uint_as_float(o[8 * g + 1]) * inv_l);
+              u.y = In16<TIn>::pack2(__uint_as_float(o[8 * g + 2]) * inv_l,
+                                     __uint_as_float(o[8 * g + 3]) * inv_l);
+              u.z = In16<TIn>::pack2(__uint_as_float(o[8 * g + 4]) * inv_l,
+                                     __uint_as_float(o[8 * g + 5]) * inv_l);
+              u.w = In16<TIn>::pack2(__uint_as_float(o[8 * g + 6]) * inv_l,
+                                     __uint_as_float(o[8 * g + 7]) * inv_l);
               d4[g] = u;
             }
           }
         }
         if (row_ok && p.lse)
-          p.lse[((int64_t)b * p.Hq + h[slot]) * p.Sq + i] = (m + log2f(l)) * 0.69314718055994531f;
+          p.lse[((int64_t)b * p.Hq + hq) * p.Sq + i] = (m_used + log2f(l)) * 0.69314718055994531f;
       }
     }
   } else if (warp < 12) {
     // =============================================================== rotation
+    setmaxnreg_inc<kRegRotate>();
     const int t = threadIdx.x - kWarpRot * 32;
+    const bool full_rot = p.apply_rope && p.rot_dim == D;
     const TIn *qbase = static_cast<const TIn *>(p.q);
     const TIn *kbase = static_cast<const TIn *>(p.k) + b * p.sk0 + hk * p.sk1;
+#pragma unroll 1
     for (int s = 0; s < 2; ++s) {
-      if (!act[s]) continue;
-      const int64_t i = m0[s] + t;
-      const bool valid = i < p.Sq;
-      const TIn *src = qbase + b * p.sq0 + h[s] * p.sq1 + (valid ? i : 0) * p.sq2;
-      rotate_row<D, TIn>(src, valid, p.kv_off + i, smem + C::OFF_Q + s * C::TILE, t, p);
+      const bool act = s ? act1 : act0;
+      if (!act) continue;
+      const int64_t m0 = s ? m01 : m00;
+      const int hq = s ? h1 : h0;
+      uint8_t *qtile = smem + C::OFF_Q + s * C::TILE;
+      if (full_rot) {
+        const TIn *rows = qbase + b * p.sq0 + hq * p.sq1 + m0 * p.sq2;
+        if (p.layout == RA_NEOX)
+          rotate_tile_full<D, TIn, RA_NEOX>(rows, p.sq2, p.Sq - m0, p.kv_off + m0, qtile, t, p);
+        else
+          rotate_tile_full<D, TIn, RA_GPTJ>(rows, p.sq2, p.Sq - m0, p.kv_off + m0, qtile, t, p);
+      } else {
+        const int64_t i = m0 + t;
+        const bool valid = i < p.Sq;
+        const TIn *src = qbase + b * p.sq0 + hq * p.sq1 + (valid ? i : 0) * p.sq2;
+        rotate_row<D, TIn>(src, valid, p.kv_off + i, qtile, t, p);
+      }
       fence_proxy_async_smem();
       mbar_arrive(bar(C::B_QFULL + s));
     }
-    for (int n = 0; n < N; ++n) {
-      const int st = n % C::NS;
-      if (n >= C::NS && !wait_bar(bar(C::B_KEMPTY + st), (uint32_t)((n / C::NS - 1) & 1), ctl))
-        break;
-      const int64_t j = (int64_t)n * 128 + t;
-      const bool valid = j < p.Sk;
-      rotate_row<D, TIn>(kbase + (valid ? j : 0) * p.sk2, valid, j, smem + C::OFF_K + st * C::TILE,
-                         t, p);
-      fence_proxy_async_smem();
-      mbar_arrive(bar(C::B_KFULL + st));
-    }
-  } else if (warp == kWarpTma) {
-    // ==================================================================== TMA
-    if (lane == 0) {
-      int issued = 0;
+    if (full_rot) {
+      if (p.layout == RA_NEOX)
+        rotate_k_loop<D, TIn, RA_NEOX, C::NS>(kbase, p, N, t, smem + C::OFF_K, bar(C::B_KFULL),
+                                             bar(C::B_KEMPTY), ctl);
+      else
+        rotate_k_loop<D, TIn, RA_GPTJ, C::NS>(kbase, p, N, t, smem + C::OFF_K, bar(C::B_KFULL),
+                                             bar(C::B_KEMPTY), ctl);
+    } else {
       for (int n = 0; n < N; ++n) {
         const int st = n % C::NS;
-        if (n >= C::NS && !wait_bar(bar(C::B_VEMPTY + st), (uint32_t)((n / C::NS - 1) & 1), ctl))
+        if (n >= C::NS && !wait_bar(bar(C::B_KEMPTY + st), (uint32_t)((n / C::NS - 1) & 1), ctl))
           break;
-        mbar_arrive_expect_tx(bar(C::B_VFULL + st), (uint32_t)C::TILE);
-        const int logical[3] = {n * 128, hk, b};
-        const int c1 = logical[p.vperm[0]], c2 = logical[p.vperm[1]], c3 = logical[p.vperm[2]];
-#pragma unroll
-        for (int sub = 0; sub < D / 64; ++sub)
-          tma_load_4d(sbase + C::OFF_V + st * C::TILE + sub * C::SUBT, &tmap_v,
-                      bar(C::B_VFULL + st), sub * 64, c1, c2, c3);
-        issued = n + 1;
-      }
-      if (*abort_flag) {  // let copies already in flight land before the block exits
-        for (int n = max(0, issued - C::NS); n < issued; ++n)
-          wait_bar_drain(bar(C::B_VFULL + n % C::NS), (uint32_t)((n / C::NS) & 1));
+        const int64_t j = (int64_t)n * 128 + t;
+        const bool valid = j < p.Sk;
+        rotate_row<D, TIn>(kbase + (valid ? j : 0) * p.sk2, valid, j,
+                           smem + C::OFF_K + st * C::TILE, t, p);
+        fence_proxy_async_smem();
+        mbar_arrive(bar(C::B_KFULL + st));
       }
     }
   } else {
-    // ==================================================================== MMA
-    if (lane == 0) {
-      constexpr uint32_t tin_bf16 = std::is_same<TIn, __nv_bfloat16>::value ? 1u : 0u;
-      constexpr uint32_t IDESC_S = idesc_f16(0u, 0u, 128);      // fp16 x fp16, K-major B
-      constexpr uint32_t IDESC_PV = idesc_f16(tin_bf16, 1u, D);  // P x V, V N-major
-      const uint32_t q_addr[2] = {sbase + C::OFF_Q, sbase + C::OFF_Q + C::TILE};
-      auto mma_s = [&](int s, int st) {
-        const uint32_t kaddr = sbase + C::OFF_K + st * C::TILE;
+    setmaxnreg_dec<kRegCtrl>();
+    if (warp == kWarpTma) {
+      // ================================================================== TMA
+      if (lane == 0) {
+        int issued = 0;
+        for (int n = 0; n < N; ++n) {
+          const int st = n % C::NS;
+          if (n >= C::NS &&
+              !wait_bar(bar(C::B_VEMPTY + st), (uint32_t)((n / C::NS - 1) & 1), ctl))
+            break;
+          mbar_arrive_expect_tx(bar(C::B_VFULL + st), (uint32_t)C::TILE);
+          const int c1 = p.vperm[0] == 0 ? n * 128 : (p.vperm[0] == 1 ? hk : b);
+          const int c2 = p.vperm[1] == 0 ? n * 128 : (p.vperm[1] == 1 ? hk : b);
+          const int c3 = p.vperm[2] == 0 ? n * 128 : (p.vperm[2] == 1 ? hk : b);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::SUBT + (kk & 3) * 32;
-          mma_ss(tmem + C::s_col(s), sdesc_sw128(q_addr[s] + off, 16, 1024),
-                 sdesc_sw128(kaddr + off, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
+          for (int sub = 0; sub < D / 64; ++sub)
+            tma_load_4d(sbase + C::OFF_V + st * C::TILE + sub * C::SUBT, &tmap_v,
+                        bar(C::B_VFULL + st), sub * 64, c1, c2, c3);
+          issued = n + 1;
         }
-      };
-      auto mma_pv = [&](int s, int st, bool acc) {
-        const uint32_t vaddr = sbase + C::OFF_V + st * C::TILE;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + C::o_col(s), tmem + C::s_col(s) + kk * 8,
-                 sdesc_sw128(vaddr + kk * 2048, C::SUBT, 1024), IDESC_PV,
-                 (acc || kk > 0) ? 1u : 0u);
-      };
-      auto part = [&](int s, int n) { return n < nend[s]; };
-      bool ok = true;
-      for (int s = 0; s < 2 && ok; ++s)
-        if (act[s]) ok = wait_bar(bar(C::B_QFULL + s), 0u, ctl);
-      if (ok && N > 0) ok = wait_bar(bar(C::B_KFULL + 0), 0u, ctl);
-      if (ok && N > 0) {
-        for (int s = 0; s < 2; ++s)
-          if (part(s, 0)) {
-            mma_s(s, 0);
-            tc_commit(bar(C::B_SFULL + s));
-          }
-        tc_commit(bar(C::B_KEMPTY + 0));
+        if (*abort_flag) {  // let copies already in flight land before the block exits
+          for (int n = max(0, issued - C::NS); n < issued; ++n)
+            wait_bar_drain(bar(C::B_VFULL + n % C::NS), (uint32_t)((n / C::NS) & 1));
+        }
       }
-      for (int n = 0; ok && n < N; ++n) {
-        const int st = n % C::NS, nst = (n + 1) % C::NS;
-        if (!wait_bar(bar(C::B_VFULL + st), (uint32_t)((n / C::NS) & 1), ctl)) { ok = false; break; }
-        bool k_next = false;
-        for (int s = 0; s < 2; ++s) {
-          if (!part(s, n)) continue;
-          if (!wait_bar(bar(C::B_PFULL + s), (uint32_t)(n & 1), ctl)) { ok = false; break; }
-          tc_fence_after();
-          mma_pv(s, st, n > 0);
-          if (n == nend[s] - 1) tc_commit(bar(C::B_OFULL + s));
-          if (part(s, n + 1)) {
-            if (!k_next) {
-              if (!wait_bar(bar(C::B_KFULL + nst), (uint32_t)(((n + 1) / C::NS) & 1), ctl)) {
-                ok = false;
-                break;
-              }
-              k_next = true;
+    } else if (warp == kWarpMma) {
+      // ================================================================== MMA
+      if (lane == 0) {
+        constexpr uint32_t tin_bf16 = std::is_same<TIn, __nv_bfloat16>::value ? 1u : 0u;
+        constexpr uint32_t IDESC_S = idesc_f16(0u, 0u, 128);      // fp16 x fp16, K-major B
+        constexpr uint32_t IDESC_PV = idesc_f16(tin_bf16, 1u, D);  // P x V, V N-major
+        auto mma_s = [&](int s, int st) {
+          const uint32_t qaddr = sbase + C::OFF_Q + s * C::TILE;
+          const uint32_t kaddr = sbase + C::OFF_K + st * C::TILE;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::SUBT + (kk & 3) * 32;
+            mma_ss(tmem + C::s_col(s), sdesc_sw128(qaddr + off, 16, 1024),
+                   sdesc_sw128(kaddr + off, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
+          }
+        };
+        auto mma_pv = [&](int s, int st, bool acc) {
+          const uint32_t vaddr = sbase + C::OFF_V + st * C::TILE;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tmem + C::o_col(s), tmem + C::s_col(s) + kk * 8,
+                   sdesc_sw128(vaddr + kk * 2048, C::SUBT, 1024), IDESC_PV,
+                   (acc || kk > 0) ? 1u : 0u);
+        };
+        auto part = [&](int s, int n) { return n < (s ? nend1 : nend0); };
+        bool ok = true;
+        if (act0) ok = wait_bar(bar(C::B_QFULL + 0), 0u, ctl);
+        if (ok && act1) ok = wait_bar(bar(C::B_QFULL + 1), 0u, ctl);
+        if (ok && N > 0) ok = wait_bar(bar(C::B_KFULL + 0), 0u, ctl);
+        if (ok && N > 0) {
+          for (int s = 0; s < 2; ++s)
+            if (part(s, 0)) {
+              mma_s(s, 0);
+              tc_commit(bar(C::B_SFULL + s));
             }
-            mma_s(s, nst);
-            tc_commit(bar(C::B_SFULL + s));
-          }
+          tc_commit(bar(C::B_KEMPTY + 0));
         }
-        if (!ok) break;
-        tc_commit(bar(C::B_VEMPTY + st));
-        if (k_next) tc_commit(bar(C::B_KEMPTY + nst));
+        for (int n = 0; ok && n < N; ++n) {
+          const int st = n % C::NS, nst = (n + 1) % C::NS;
+          if (!wait_bar(bar(C::B_VFULL + st), (uint32_t)((n / C::NS) & 1), ctl)) { ok = false; break; }
+          bool k_next = false;
+          for (int s = 0; s < 2; ++s) {
+            if (!part(s, n)) continue;
+            if (!wait_bar(bar(C::B_PFULL + s), (uint32_t)(n & 1), ctl)) { ok = false; break; }
+            tc_fence_after();
+            mma_pv(s, st, n > 0);
+            if (n == (s ? nend1 : nend0) - 1) tc_commit(bar(C::B_OFULL + s));
+            if (part(s, n + 1)) {
+              if (!k_next) {
+                if (!wait_bar(bar(C::B_KFULL + nst), (uint32_t)(((n + 1) / C::NS) & 1), ctl)) {
+                  ok = false;
+                  break;
+                }
+                k_next = true;
+              }
+              mma_s(s, nst);
+              tc_commit(bar(C::B_SFULL + s));
+            }
+          }
+          if (!ok) break;
+          tc_commit(bar(C::B_VEMPTY + st));
+          if (k_next) tc_commit(bar(C::B_KEMPTY + nst));
+        }
+        // all issued MMAs complete before tensor memory is released
+        tc_commit(bar(C::B_DONE));
+        wait_bar_drain(bar(C::B_DONE), 0u);
       }
-      // all issued MMAs complete before tensor memory is released
-      tc_commit(bar(C::B_DONE));
-      wait_bar_drain(bar(C::B_DONE), 0u);
     }
   }
 
@@ -604,6 +824,11 @@ cudaError_t launch_typed(const AttnArgs &a, const CUtensorMap &map, const TcPara
   std::call_once(once, [] {
     attr_err = cudaFuncSetAttribute(attn_tc_kernel<D, TIn>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    // The setmaxnreg shares add up to 512 threads x 128 registers: a build
+    // that allocated anything else could leave an increase waiting forever.
+    cudaFuncAttributes fa;
+    if (attr_err == cudaSuccess) attr_err = cudaFuncGetAttributes(&fa, attn_tc_kernel<D, TIn>);
+    if (attr_err == cudaSuccess && fa.numRegs != 128) attr_err = cudaErrorInvalidConfiguration;
   });
   if (attr_err != cudaSuccess) return attr_err;
   attn_tc_kernel<D, TIn><<<grid, kThreads, C::SMEM, s>>>(map, p);
@@ -629,7 +854,7 @@ cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t s) {
   p.n_units = a.B * p.units_per_b;
   p.n_qt = (int)(p.pack_heads ? (a.Sq + 127) / 128 : (a.Sq + 255) / 256);
   p.apply_rope = a.apply_rope; p.rot_dim = a.rot_dim; p.layout = a.layout;
-  p.cos_t = a.cos_t; p.sin_t = a.sin_t;
+  p.cos_t = a.cos_t; p.sin_t = a.sin_t; p.table_rows = a.table_rows;
   p.scale_log2 = (float)((double)a.scale * 1.4426950408889634);
   p.status = a.status;
   const int64_t grid = (int64_t)p.n_qt * p.n_units;
