@@ -497,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 8) {
     // ================================================================ softmax
-    setmaxnreg_inc<kRegSoftmax>();
+    setmaxnreg_to<128, kRegSoftmax>();
     const int slot = warp >> 2;
     const int wq = warp & 3;
     const int t = wq * 32 + lane;
@@ -611,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < 12) {
     // =============================================================== rotation
-    setmaxnreg_inc<kRegRotate>();
+    setmaxnreg_to<128, kRegRotate>();
     const int t = threadIdx.x - kWarpRot * 32;
     const bool full_rot = p.apply_rope && p.rot_dim == D;
     const TIn *qbase = static_cast<const TIn *>(p.q);
@@ -659,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    setmaxnreg_dec<kRegCtrl>();
+    setmaxnreg_to<128, kRegCtrl>();
     if (warp == kWarpTma) {
       // ================================================================== TMA
       if (lane == 0) {
@@ -690,22 +690,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint32_t tin_bf16 = std::is_same<TIn, __nv_bfloat16>::value ? 1u : 0u;
         constexpr uint32_t IDESC_S = idesc_f16(0u, 0u, 128);      // fp16 x fp16, K-major B
         constexpr uint32_t IDESC_PV = idesc_f16(tin_bf16, 1u, D);  // P x V, V N-major
+        // descriptor low words of every tile base, computed once; each K=16
+        // step then adds a constant ((offset >> 4) of the step)
+        constexpr uint32_t HI = sdesc_hi_sw128(1024);
+        const uint32_t q_lo0 = sdesc_lo(sbase + C::OFF_Q, 16);
+        const uint32_t k_lo0 = sdesc_lo(sbase + C::OFF_K, 16);
+        const uint32_t v_lo0 = sdesc_lo(sbase + C::OFF_V, C::SUBT);
         auto mma_s = [&](int s, int st) {
-          const uint32_t qaddr = sbase + C::OFF_Q + s * C::TILE;
-          const uint32_t kaddr = sbase + C::OFF_K + st * C::TILE;
+          const uint32_t qlo = q_lo0 + (uint32_t)(s * C::TILE >> 4);
+          const uint32_t klo = k_lo0 + (uint32_t)(st * C::TILE >> 4);
+          const uint32_t dS = tmem + C::s_col(s);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * C::SUBT + (kk & 3) * 32;
-            mma_ss(tmem + C::s_col(s), sdesc_sw128(qaddr + off, 16, 1024),
-                   sdesc_sw128(kaddr + off, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
+            const uint32_t off = ((kk >> 2) * C::SUBT + (kk & 3) * 32) >> 4;
+            mma_ss(dS, sdesc_join(qlo + off, HI), sdesc_join(klo + off, HI), IDESC_S,
+                   kk > 0 ? 1u : 0u);
           }
         };
         auto mma_pv = [&](int s, int st, bool acc) {
-          const uint32_t vaddr = sbase + C::OFF_V + st * C::TILE;
+          const uint32_t vlo = v_lo0 + (uint32_t)(st * C::TILE >> 4);
+          const uint32_t dO = tmem + C::o_col(s), aP = tmem + C::s_col(s);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tmem + C::o_col(s), tmem + C::s_col(s) + kk * 8,
-                   sdesc_sw128(vaddr + kk * 2048, C::SUBT, 1024), IDESC_PV,
+            mma_ts(dO, aP + kk * 8, sdesc_join(vlo + (uint32_t)(kk * 2048 >> 4), HI), IDESC_PV,
                    (acc || kk > 0) ? 1u : 0u);
         };
         auto part = [&](int s, int n) { return n < (s ? nend1 : nend0); };

@@ -192,6 +192,27 @@ template <uint32_t N> __device__ __forceinline__ void setmaxnreg_inc() {
 template <uint32_t N> __device__ __forceinline__ void setmaxnreg_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
+// Moves this warpgroup from the launch allocation `From` to `To` registers per
+// thread: an increase or a decrease as the values require (an increase to a
+// smaller count, or a decrease to a larger one, is not a valid request).
+template <uint32_t From, uint32_t To> __device__ __forceinline__ void setmaxnreg_to() {
+  static_assert(To % 8 == 0 && To >= 24 && To <= 256, "setmaxnreg range");
+  if constexpr (To > From) setmaxnreg_inc<To>();
+  else if constexpr (To < From) setmaxnreg_dec<To>();
+}
+
+// Descriptor split into a constant high word and a low word holding the start
+// address (and leading byte offset), so per-step offsets are one 32-bit add.
+__device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr >> 4) & 0x3FFFu) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+// High word for the 128-byte swizzle with stride byte offset `sbo`.
+__host__ __device__ constexpr uint32_t sdesc_hi_sw128(uint32_t sbo) {
+  return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+__device__ __forceinline__ uint64_t sdesc_join(uint32_t lo, uint32_t hi) {
+  return ((uint64_t)hi << 32) | lo;
+}
 
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
