@@ -63,6 +63,18 @@ def peaks():
         return 6800.0, 1900.0, "fallback"
 
 
+def max_over_ranks(value: float) -> float:
+    """Max of a per-rank float over all ranks (identity without a process
+    group); CUDA tensor under NCCL, CPU tensor under gloo."""
+    dist = torch.distributed
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def src_hash(path):
     with open(path, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
@@ -237,11 +249,7 @@ def time_attention(ra, W, args, dev, stream, ws, local, host_e2e=True):
         torch.distributed.barrier()
     if ra.ra_get_device_status() != 0:
         raise RuntimeError("device status error during timed steps")
-    ms = statistics.mean(a.elapsed_time(b) for a, b in zip(starts, ends))
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in zip(starts, ends)))
     out = {"ms": ms, "wall": wall, "clocks": clk.summary(), "flops": W.flops()}
     if host_e2e:
         # the same call through host buffers: H2D of q, k, v and D2H of O, LSE each step
@@ -295,6 +303,59 @@ def time_rope(ra, args, dev, stream):
     return {"ms": ms, "bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9, "T": T}
 
 
+def run_sweep(ra, args, dev, stream, rank, tf_peak, hbm_peak):
+    """One line per workload: attention TFLOP/s (L2 flushed per call, CUDA
+    events, median) and rope GB/s; not the bench line."""
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    for W in wl.ALL_ATTN:
+        q, k, v = [t.to(dev) for t in W.inputs()]
+        cos, sin = ra.make_tables(max(W.Sk, W.kv_offset + W.Sq), W.r, W.base, device=dev)
+        scale = 1.0 / 8 if W is wl.FP32_ATTN else None
+        call = lambda: ra.attn_fwd_causal_rope(q, k, v, cos, sin, kv_offset=W.kv_offset,
+                                               layout=W.layout, softmax_scale=scale)
+        for _ in range(args.warmup):
+            call()
+        ts = []
+        for _ in range(args.steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        ms = statistics.median(ts)
+        tf = W.flops() / (ms * 1e-3) / 1e12
+        if rank == 0:
+            print(json.dumps({"workload": W.name, "ms": ms, "TFLOP/s": tf,
+                              "frac_of_bf16_peak": tf / tf_peak}), flush=True)
+    for R in wl.ALL_ROPE:
+        rq, rk = [t.to(dev) for t in R.inputs()]
+        pos = torch.from_numpy(R.positions()).to(torch.int32).to(dev)
+        cos, sin = ra.make_tables(R.table_rows, R.rot_dim, R.base, device=dev)
+        call = lambda: ra.rope_apply_qk(rq, rk, pos, cos, sin, layout=R.layout)
+        for _ in range(args.warmup):
+            call()
+        ts = []
+        for _ in range(args.steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        ms = statistics.median(ts)
+        gbs = R.algorithmic_bytes() / (ms * 1e-3) / 1e9
+        if rank == 0:
+            print(json.dumps({"workload": R.name, "ms": ms, "GB/s": gbs,
+                              "frac_of_hbm": gbs / hbm_peak, "l2": "flushed per call"}),
+                  flush=True)
+    if ra.ra_get_device_status() != 0:
+        raise RuntimeError("device status error in sweep")
+    return 0
+
+
 def run_ours(args, ws, rank, local):
     import rope_causal_attention_gb300 as ra
     from rope_causal_attention_gb300 import build as rbuild
@@ -307,6 +368,8 @@ def run_ours(args, ws, rank, local):
     stream = torch.cuda.current_stream(dev)
     hbm_peak, tf_peak, peak_kind = peaks()
 
+    if args.sweep:
+        return run_sweep(ra, args, dev, stream, rank, tf_peak, hbm_peak)
     if args.only == "rope":
         r = time_rope(ra, args, dev, stream)
         if rank == 0:
@@ -378,6 +441,9 @@ def main():
     ap.add_argument("--attn-sq", type=int, default=0,
                     help="profiling aid: shrink the attention workload to this many new "
                          "queries (the 4096-row cached prefix is kept)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="report: time every attention workload (fp32, the GPT-J sweep, "
+                         "long-context GQA) and both rope workloads, one JSON line each")
     ap.add_argument("--rope-tokens", type=int, default=0,
                     help="profiling aid: rotate only the first N tokens of the batch")
     args = ap.parse_args()

@@ -40,6 +40,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <math.h>
+#include <stdlib.h>
 
 #include <algorithm>
 #include <mutex>
@@ -100,6 +101,7 @@ struct TcParams {
   float scale_log2;
   int vperm[3];  // tensor-map dims 1..3 -> logical coordinate (0 key row, 1 kv head, 2 batch)
   int *status;
+  int withhold_v0;  // failure-detection test: never load V tile 0 (see launch_attn_tc)
 };
 
 struct Ctl {
@@ -664,11 +666,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ================================================================== TMA
       if (lane == 0) {
         int issued = 0;
+        const int first_real = p.withhold_v0 ? 1 : 0;  // tiles below this are never loaded
         for (int n = 0; n < N; ++n) {
           const int st = n % C::NS;
           if (n >= C::NS &&
               !wait_bar(bar(C::B_VEMPTY + st), (uint32_t)((n / C::NS - 1) & 1), ctl))
             break;
+          if (n < first_real) continue;
           mbar_arrive_expect_tx(bar(C::B_VFULL + st), (uint32_t)C::TILE);
           const int c1 = p.vperm[0] == 0 ? n * 128 : (p.vperm[0] == 1 ? hk : b);
           const int c2 = p.vperm[1] == 0 ? n * 128 : (p.vperm[1] == 1 ? hk : b);
@@ -680,7 +684,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           issued = n + 1;
         }
         if (*abort_flag) {  // let copies already in flight land before the block exits
-          for (int n = max(0, issued - C::NS); n < issued; ++n)
+          for (int n = max(first_real, issued - C::NS); n < issued; ++n)
             wait_bar_drain(bar(C::B_VFULL + n % C::NS), (uint32_t)((n / C::NS) & 1));
         }
       }
@@ -864,6 +868,14 @@ cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t s) {
   p.cos_t = a.cos_t; p.sin_t = a.sin_t; p.table_rows = a.table_rows;
   p.scale_log2 = (float)((double)a.scale * 1.4426950408889634);
   p.status = a.status;
+  // Failure-detection test hook: with RA_TEST_WITHHOLD_V_TILE0=1 in the
+  // environment the TMA producer never loads V tile 0, so the MMA issuer's
+  // bounded wait runs out and the launch must end with RA_ERR_DEVICE_TIMEOUT
+  // in the status word and a usable context.  Nothing else reads it.
+  {
+    const char *w = getenv("RA_TEST_WITHHOLD_V_TILE0");
+    p.withhold_v0 = (w && w[0] == '1') ? 1 : 0;
+  }
   const int64_t grid = (int64_t)p.n_qt * p.n_units;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
