@@ -10,13 +10,14 @@
 //   Positions come from positions[t]; dims past rot_dim stay untouched.
 //
 // GB300 design: the rotation is a pure stream (read Q/K once, write once), so
-// it is bound by HBM bandwidth.  Each thread owns one 16-byte slice of one
-// head (NeoX: a 16-byte piece of the low half plus the matching piece of the
-// high half; GPT-J: 16 contiguous bytes, i.e. whole pairs).  A block holds one
-// token: threadIdx.x = slice, threadIdx.y = head, so a warp touches
-// consecutive slices of consecutive heads -- contiguous 128-bit accesses.  The
-// token's cos/sin slice is loaded once per thread through the read-only path
-// and reused for every head that thread visits; Q and K heads share one launch.
+// it is bound by HBM bandwidth.  Each thread owns one 16-byte slice (NeoX: a
+// 16-byte piece of the low half plus the matching piece of the high half;
+// GPT-J: 16 contiguous bytes, i.e. whole pairs) of up to four heads of one
+// token: threadIdx.x = slice, threadIdx.y = head group, threadIdx.z = token
+// within the block, so a warp touches consecutive slices of consecutive heads
+// -- contiguous 128-bit accesses.  A thread issues all its heads' loads before
+// its first store, and loads the token's cos/sin slice once (read-only path)
+// for all of them; Q and K heads share one launch.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -89,62 +90,89 @@ __device__ __forceinline__ void load_table(const float *__restrict__ p, float *o
   }
 }
 
+// Heads handled by one thread per token, loaded together before any store
+// (in place, a store may alias a later head's load, so the compiler cannot
+// overlap heads on its own).
+constexpr int kHeadsPerThread = 4;
+
 template <typename T, int LAYOUT>
-__global__ void __launch_bounds__(1024) rope_apply_vec_kernel(RopeKParams p) {
+__global__ void __launch_bounds__(512) rope_apply_vec_kernel(RopeKParams p) {
   constexpr int V = VecN<T>::N;                         // elements per 16 bytes
   constexpr int NP = (LAYOUT == RA_NEOX) ? V : V / 2;   // pairs per slice
+  constexpr int NH = kHeadsPerThread;
+  constexpr int LD = (LAYOUT == RA_NEOX) ? 2 : 1;       // 16-byte loads per head
   const int s = threadIdx.x;
-  for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x) {
+  const int hy = blockDim.y;  // heads of a token are h = threadIdx.y + k * hy, k < NH
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.z + threadIdx.z; t < p.T;
+       t += (int64_t)gridDim.x * blockDim.z) {
     const int64_t pos = load_position(p.positions, p.is64, t);
     if (pos < 0 || pos >= p.table_rows) {
       if (s == 0 && threadIdx.y == 0) record_status(p.status, RA_ERR_POSITION_RANGE);
       continue;
     }
+    const T *src[NH];
+    T *dst[NH];
+    bool ok[NH];
+#pragma unroll
+    for (int k = 0; k < NH; ++k) {
+      const int h = threadIdx.y + k * hy;
+      ok[k] = h < p.Htot;
+      const bool isq = h < p.Hq;
+      const int hh = isq ? h : h - p.Hq;
+      src[k] = static_cast<const T *>(isq ? p.q : p.k) + t * (isq ? p.sq_t : p.sk_t) +
+               hh * (isq ? p.sq_h : p.sk_h);
+      dst[k] = static_cast<T *>(isq ? p.qo : p.ko) + t * (isq ? p.sqo_t : p.sko_t) +
+               hh * (isq ? p.sqo_h : p.sko_h);
+    }
     if (s < p.s_rot) {
       const int i0 = s * NP;  // first pair index of this slice
+      // NeoX: low-half and high-half pieces; GPT-J: whole pairs
+      const int off0 = (LAYOUT == RA_NEOX) ? i0 : 2 * i0;
+      const int off1 = i0 + p.half;
+      uint4 raw[NH][LD];
+#pragma unroll
+      for (int k = 0; k < NH; ++k) {
+        if (!ok[k]) continue;
+        raw[k][0] = *reinterpret_cast<const uint4 *>(src[k] + off0);
+        if (LD == 2) raw[k][LD - 1] = *reinterpret_cast<const uint4 *>(src[k] + off1);
+      }
       float c[NP], sn[NP];
       load_table<NP>(p.cos_t + pos * p.half + i0, c);
       load_table<NP>(p.sin_t + pos * p.half + i0, sn);
-      for (int h = threadIdx.y; h < p.Htot; h += blockDim.y) {
-        const bool isq = h < p.Hq;
-        const int hh = isq ? h : h - p.Hq;
-        const T *src = static_cast<const T *>(isq ? p.q : p.k) +
-                       t * (isq ? p.sq_t : p.sk_t) + hh * (isq ? p.sq_h : p.sk_h);
-        T *dst = static_cast<T *>(isq ? p.qo : p.ko) + t * (isq ? p.sqo_t : p.sko_t) +
-                 hh * (isq ? p.sqo_h : p.sko_h);
+#pragma unroll
+      for (int k = 0; k < NH; ++k) {
+        if (!ok[k]) continue;
         if constexpr (LAYOUT == RA_NEOX) {
           float lo[V], hi[V], olo[V], ohi[V];
-          unpack16<T>(*reinterpret_cast<const uint4 *>(src + i0), lo);
-          unpack16<T>(*reinterpret_cast<const uint4 *>(src + p.half + i0), hi);
+          unpack16<T>(raw[k][0], lo);
+          unpack16<T>(raw[k][LD - 1], hi);
 #pragma unroll
           for (int j = 0; j < V; ++j) {
             olo[j] = lo[j] * c[j] - hi[j] * sn[j];
             ohi[j] = hi[j] * c[j] + lo[j] * sn[j];
           }
-          *reinterpret_cast<uint4 *>(dst + i0) = pack16<T>(olo);
-          *reinterpret_cast<uint4 *>(dst + p.half + i0) = pack16<T>(ohi);
+          *reinterpret_cast<uint4 *>(dst[k] + off0) = pack16<T>(olo);
+          *reinterpret_cast<uint4 *>(dst[k] + off1) = pack16<T>(ohi);
         } else {
           float x[V], y[V];
-          unpack16<T>(*reinterpret_cast<const uint4 *>(src + 2 * i0), x);
+          unpack16<T>(raw[k][0], x);
 #pragma unroll
           for (int j = 0; j < NP; ++j) {
             y[2 * j] = x[2 * j] * c[j] - x[2 * j + 1] * sn[j];
             y[2 * j + 1] = x[2 * j + 1] * c[j] + x[2 * j] * sn[j];
           }
-          *reinterpret_cast<uint4 *>(dst + 2 * i0) = pack16<T>(y);
+          *reinterpret_cast<uint4 *>(dst[k] + off0) = pack16<T>(y);
         }
       }
     } else if (s < p.s_rot + p.s_tail) {  // out of place: copy the unrotated tail
       const int e0 = p.rot_dim + (s - p.s_rot) * V;
-      for (int h = threadIdx.y; h < p.Htot; h += blockDim.y) {
-        const bool isq = h < p.Hq;
-        const int hh = isq ? h : h - p.Hq;
-        const T *src = static_cast<const T *>(isq ? p.q : p.k) +
-                       t * (isq ? p.sq_t : p.sk_t) + hh * (isq ? p.sq_h : p.sk_h);
-        T *dst = static_cast<T *>(isq ? p.qo : p.ko) + t * (isq ? p.sqo_t : p.sko_t) +
-                 hh * (isq ? p.sqo_h : p.sko_h);
-        *reinterpret_cast<uint4 *>(dst + e0) = *reinterpret_cast<const uint4 *>(src + e0);
-      }
+      uint4 raw[NH];
+#pragma unroll
+      for (int k = 0; k < NH; ++k)
+        if (ok[k]) raw[k] = *reinterpret_cast<const uint4 *>(src[k] + e0);
+#pragma unroll
+      for (int k = 0; k < NH; ++k)
+        if (ok[k]) *reinterpret_cast<uint4 *>(dst[k] + e0) = raw[k];
     }
   }
 }
@@ -197,10 +225,17 @@ int sm_count() {
 template <typename T>
 cudaError_t launch_vec(const RopeKParams &kp, ra_layout layout, cudaStream_t s) {
   const int slices = kp.s_rot + kp.s_tail;
-  const int hy = (kp.Htot * slices <= 1024) ? kp.Htot : (1024 / slices);
-  const dim3 block(slices, hy > 0 ? hy : 1);
+  // every head of a token must be reachable: blockDim.y * kHeadsPerThread >= Htot
+  const int hy = (kp.Htot + kHeadsPerThread - 1) / kHeadsPerThread;
+  if (slices * hy > 512) return cudaErrorNotSupported;
+  // several tokens per block (z) so that a block has ~256 threads
+  int tz = 256 / (slices * hy);
+  if (tz < 1) tz = 1;
+  if (tz > 64) tz = 64;
+  const dim3 block(slices, hy, tz);
   const int64_t max_grid = (int64_t)sm_count() * 64;
-  const unsigned grid = (unsigned)(kp.T < max_grid ? kp.T : max_grid);
+  const int64_t need = (kp.T + tz - 1) / tz;
+  const unsigned grid = (unsigned)(need < max_grid ? need : max_grid);
   if (layout == RA_NEOX)
     rope_apply_vec_kernel<T, RA_NEOX><<<grid, block, 0, s>>>(kp);
   else
@@ -258,6 +293,10 @@ cudaError_t launch_rope_apply(const RopeArgs &a, bool vectorized, cudaStream_t s
     const int V = 16 / es;
     kp.s_rot = a.layout == RA_NEOX ? kp.half / V : a.rot_dim / V;
     kp.s_tail = tail / V;
+    const int hy = (kp.Htot + kHeadsPerThread - 1) / kHeadsPerThread;
+    vectorized = (kp.s_rot + kp.s_tail) * hy <= 512;  // else the scalar kernel
+  }
+  if (vectorized) {
     switch (a.dt) {
       case RA_F32: return launch_vec<float>(kp, a.layout, s);
       case RA_BF16: return launch_vec<__nv_bfloat16>(kp, a.layout, s);
