@@ -355,6 +355,40 @@ def run_sweep(ra, args, dev, stream, rank, tf_peak, hbm_peak):
             print(json.dumps({"workload": W.name, "ms": ms, "TFLOP/s": tf,
                               "frac_of_bf16_peak": tf / tf_peak, "warm_ms": warm,
                               "warm_TFLOP/s": W.flops() / (warm * 1e-3) / 1e12}), flush=True)
+    # P1's comparison on GB300: plain flash, rotate-then-flash, fused; device
+    # time per call (graph-replayed) and peak extra memory of one call
+    for W in wl.SWEEP:
+        q, k, v = [t.to(dev) for t in W.inputs()]
+        cos, sin = ra.make_tables(W.Sk, W.r, W.base, device=dev)
+
+        def flash():
+            return ra.attn_fwd_causal_rope(q, k, v, apply_rope=False)
+
+        def unfused():
+            qr = torch.empty_like(q)
+            kr = torch.empty_like(k)
+            for b in range(W.B):  # [H, S, D] of one batch viewed token-major as [S, H, D]
+                ra.rope_apply_qk(q[b].transpose(0, 1), k[b].transpose(0, 1), pos, cos, sin,
+                                 layout=W.layout, q_out=qr[b].transpose(0, 1),
+                                 k_out=kr[b].transpose(0, 1))
+            return ra.attn_fwd_causal_rope(qr, kr, v, apply_rope=False)
+
+        def fused():
+            return ra.attn_fwd_causal_rope(q, k, v, cos, sin, layout=W.layout)
+
+        pos = torch.arange(W.Sq, dtype=torch.int32, device=dev)
+        row = {"ablation": W.name}
+        for name, fn in (("flash", flash), ("rope_then_flash", unfused), ("fused", fused)):
+            fn()
+            torch.cuda.synchronize()
+            base_mem = torch.cuda.memory_allocated()
+            torch.cuda.reset_peak_memory_stats()
+            fn()
+            torch.cuda.synchronize()
+            extra = torch.cuda.max_memory_allocated() - base_mem
+            row[name] = {"warm_ms": warm_ms(fn, stream, 20), "peak_extra_MB": extra / 2 ** 20}
+        if rank == 0:
+            print(json.dumps(row), flush=True)
     for R in wl.ALL_ROPE:
         rq, rk = [t.to(dev) for t in R.inputs()]
         pos = torch.from_numpy(R.positions()).to(torch.int32).to(dev)

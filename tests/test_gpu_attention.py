@@ -190,3 +190,32 @@ def test_rejections_with_real_buffers(ra):
         ra.attn_fwd_causal_rope(q96, k96, k96, apply_rope=False)
     assert e.value.code == -2
     assert ra.ra_get_device_status() == 0
+
+
+@pytest.mark.parametrize("layout", [NEOX, GPTJ])
+def test_unfused_rotate_then_flash_matches(ra, orc, layout):
+    """The ablation path: rope_apply_qk into copies, then attention without
+    RoPE.  Each stage is checked against the oracle on its own inputs: the
+    materialised rotated Q/K (bf16, as rope_apply_qk returns them) fed to the
+    no-RoPE kernel must match the oracle's attention of those same tensors at
+    the standard tolerances, and its O must also match the fused result's
+    oracle (bf16 rounding of the rotated operands moves LSE, not O, beyond
+    the fused kernel's bound: the fused kernel keeps them in fp16)."""
+    B, H, S, D = 2, 4, 300, 64
+    q, k, v = wl.attn_qkv(B, H, H, S, S, D, torch.bfloat16, seed=31)
+    cos, sin = ra.make_tables(S, D, 10000.0)
+    qg, kg, vg = q.cuda(), k.cuda(), v.cuda()
+    qr, kr = torch.empty_like(qg), torch.empty_like(kg)
+    pos = torch.arange(S, dtype=torch.int32, device="cuda")
+    for b in range(B):
+        ra.rope_apply_qk(qg[b].transpose(0, 1), kg[b].transpose(0, 1), pos, cos, sin,
+                         layout=layout, q_out=qr[b].transpose(0, 1), k_out=kr[b].transpose(0, 1))
+    o_u, lse_u = ra.attn_fwd_causal_rope(qr, kr, vg, apply_rope=False)
+    assert ra.ra_get_device_status() == 0
+    qr_c, kr_c = qr.float().cpu().numpy(), kr.float().cpu().numpy()
+    o_ref_u, lse_ref_u = orc.attention(qr_c, kr_c, v.float().numpy(), apply_rope=False)
+    assert np.abs(o_u.float().cpu().numpy() - o_ref_u).max() <= 2e-2
+    assert np.abs(lse_u.cpu().numpy() - lse_ref_u).max() <= 1e-3
+    o_ref, _ = orc.attention(q.float().numpy(), k.float().numpy(), v.float().numpy(),
+                             layout=layout)
+    assert np.abs(o_u.float().cpu().numpy() - o_ref).max() <= 2e-2
