@@ -23,7 +23,8 @@
  * Sources (page title, section) for what each call computes:
  *  [RF] "RoPE and FlashAttention: relative positions and online softmax":
  *       1 (pair rotation, theta_i = base^(-2i/d)), 2 (absolute positions,
- *       decoder cache convention), 4 (S = QK^T/sqrt(d), P = softmax(S),
+ *       decoder cache convention), 3 (context extension: position
+ *       interpolation, larger base), 4 (S = QK^T/sqrt(d), P = softmax(S),
  *       O = PV), 5 (online softmax with running max / denominator /
  *       numerator; offset-causal mask j <= off + i).
  *  [TR] "Write Triton Rope Kernel": layouts (NeoX halves vs GPT-J pairs),
@@ -71,6 +72,17 @@ typedef enum { RA_F32 = 0, RA_BF16 = 1, RA_F16 = 2 } ra_dtype;
  */
 ra_status rope_tables_build(float *cos_out, float *sin_out, int64_t rows, int rot_dim,
                             double base, int freq_dim, cudaStream_t s);
+
+/*
+ * rope_tables_build_scaled -- tables for position interpolation: like
+ *   rope_tables_build with angle (p / pos_scale) * theta_i, i.e. positions
+ *   divided by an extension factor before the angle is formed ([RF] 3,
+ *   Position Interpolation).  pos_scale = 1 gives rope_tables_build's tables
+ *   bit for bit; NTK-style scaling needs no new call (it is a larger `base`,
+ *   whose value belongs to the checkpoint).  pos_scale must be finite and > 0.
+ */
+ra_status rope_tables_build_scaled(float *cos_out, float *sin_out, int64_t rows, int rot_dim,
+                                   double base, int freq_dim, double pos_scale, cudaStream_t s);
 
 /*
  * rope_apply_qk -- rotate Q and K of a packed token batch in one launch

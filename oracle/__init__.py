@@ -71,6 +71,8 @@ def _load():
             lib.oracle_rope_freqs.restype = None
             lib.oracle_rope_tables.argtypes = [i64, i32, i32, f64, dp, dp]
             lib.oracle_rope_tables.restype = None
+            lib.oracle_rope_tables_scaled.argtypes = [i64, i32, i32, f64, f64, dp, dp]
+            lib.oracle_rope_tables_scaled.restype = None
             lib.oracle_rope_rows.argtypes = [dp, i64, i32, lp, i32, i32, f64, i32, dp]
             lib.oracle_rope_rows.restype = i32
             lib.oracle_attention.argtypes = [fp, fp, fp, i32, i32, i32, i64, i64, i32, i64,
@@ -105,6 +107,17 @@ def rope_tables(rows: int, rot_dim: int, base: float, freq_dim: int = 0):
     s = np.empty((rows, half), dtype=np.float64)
     _load().oracle_rope_tables(rows, rot_dim, freq_dim, float(base),
                                _ptr(c, ctypes.c_double), _ptr(s, ctypes.c_double))
+    return c, s
+
+
+def rope_tables_scaled(rows: int, rot_dim: int, base: float, pos_scale: float,
+                       freq_dim: int = 0):
+    """fp64 cos and sin of (p / pos_scale) * theta_i (position interpolation)."""
+    half = rot_dim // 2
+    c = np.empty((rows, half), dtype=np.float64)
+    s = np.empty((rows, half), dtype=np.float64)
+    _load().oracle_rope_tables_scaled(rows, rot_dim, freq_dim, float(base), float(pos_scale),
+                                      _ptr(c, ctypes.c_double), _ptr(s, ctypes.c_double))
     return c, s
 
 

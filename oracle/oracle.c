@@ -103,6 +103,24 @@ void oracle_rope_tables(int64_t rows, int rot_dim, int freq_dim, double base,
   free(theta);
 }
 
+/* Position-interpolated tables: cos/sin of (p / pos_scale) * theta_i, i.e.
+ * positions divided by an extension factor before the angle is formed
+ * ("RoPE and FlashAttention ...", section 3, Position Interpolation).  With
+ * pos_scale = 1 this is oracle_rope_tables. */
+void oracle_rope_tables_scaled(int64_t rows, int rot_dim, int freq_dim, double base,
+                               double pos_scale, double *cos_out, double *sin_out) {
+  const int half = rot_dim / 2;
+  double *theta = (double *)malloc((size_t)(half > 0 ? half : 1) * sizeof(double));
+  oracle_rope_freqs(rot_dim, freq_dim, base, theta);
+  for (int64_t p = 0; p < rows; ++p)
+    for (int i = 0; i < half; ++i) {
+      const double a = ((double)p / pos_scale) * theta[i];
+      cos_out[p * half + i] = cos(a);
+      sin_out[p * half + i] = sin(a);
+    }
+  free(theta);
+}
+
 /* Rotates one row x[0..D) at integer position p into y (y may equal x).
  * NeoX pairs (i, i + rot_dim/2), GPT-J pairs (2i, 2i+1), i < rot_dim/2;
  * dims [rot_dim, D) are copied unchanged.  [TR] steps 1, 5, 6, 8. */

@@ -18,7 +18,8 @@ import threading
 
 import torch
 
-__all__ = ["NEOX", "GPTJ", "RAError", "rope_tables_build", "make_tables", "rope_apply_qk",
+__all__ = ["NEOX", "GPTJ", "RAError", "rope_tables_build", "rope_tables_build_scaled",
+           "make_tables", "rope_apply_qk",
            "attn_fwd_causal_rope", "ra_get_device_status", "ra_status_string", "library_path",
            "lib"]
 
@@ -58,6 +59,8 @@ def lib():
                                       ctypes.c_double, ctypes.c_float)
             L.rope_tables_build.argtypes = [vp, vp, i64, i32, f64, i32, vp]
             L.rope_tables_build.restype = i32
+            L.rope_tables_build_scaled.argtypes = [vp, vp, i64, i32, f64, i32, f64, vp]
+            L.rope_tables_build_scaled.restype = i32
             L.rope_apply_qk.argtypes = [vp, vp, vp, vp, i32, i64, i32, i32, i32, i32, i32,
                                         _i64p, _i64p, _i64p, _i64p, vp, i32, vp, vp, i64, vp]
             L.rope_apply_qk.restype = i32
@@ -106,26 +109,40 @@ def _cuda(t, name):
 
 
 def rope_tables_build(cos_out: torch.Tensor, sin_out: torch.Tensor, base: float,
-                      freq_dim: int = 0, stream=None):
-    """Fills fp32 tables [rows, rot_dim/2] with cos/sin(p * base^(-2i/F))."""
+                      freq_dim: int = 0, stream=None, pos_scale: float = 1.0):
+    """Fills fp32 tables [rows, rot_dim/2] with cos/sin((p / pos_scale) *
+    base^(-2i/F)); pos_scale != 1 calls rope_tables_build_scaled (position
+    interpolation)."""
     _cuda(cos_out, "cos_out")
     _cuda(sin_out, "sin_out")
     if (cos_out.dtype != torch.float32 or sin_out.shape != cos_out.shape or cos_out.dim() != 2
             or not cos_out.is_contiguous() or not sin_out.is_contiguous()):
         raise ValueError("tables must be contiguous fp32 [rows, rot_dim/2] of equal shape")
     rows, half = cos_out.shape
-    _check(lib().rope_tables_build(_ptr(cos_out), _ptr(sin_out), rows, 2 * half, float(base),
-                                   int(freq_dim), _stream(cos_out.device, stream)),
-           "rope_tables_build")
+    if pos_scale == 1.0:
+        _check(lib().rope_tables_build(_ptr(cos_out), _ptr(sin_out), rows, 2 * half, float(base),
+                                       int(freq_dim), _stream(cos_out.device, stream)),
+               "rope_tables_build")
+    else:
+        _check(lib().rope_tables_build_scaled(_ptr(cos_out), _ptr(sin_out), rows, 2 * half,
+                                              float(base), int(freq_dim), float(pos_scale),
+                                              _stream(cos_out.device, stream)),
+               "rope_tables_build_scaled")
     return cos_out, sin_out
 
 
+def rope_tables_build_scaled(cos_out, sin_out, base: float, pos_scale: float, freq_dim: int = 0,
+                             stream=None):
+    """Position-interpolated tables: cos/sin((p / pos_scale) * theta_i)."""
+    return rope_tables_build(cos_out, sin_out, base, freq_dim, stream, pos_scale)
+
+
 def make_tables(rows: int, rot_dim: int, base: float, freq_dim: int = 0, device="cuda",
-                stream=None):
+                stream=None, pos_scale: float = 1.0):
     """Allocates and builds the cos/sin tables (fp32 [rows, rot_dim/2] each)."""
     c = torch.empty((rows, rot_dim // 2), dtype=torch.float32, device=device)
     s = torch.empty_like(c)
-    return rope_tables_build(c, s, base, freq_dim, stream)
+    return rope_tables_build(c, s, base, freq_dim, stream, pos_scale)
 
 
 def rope_apply_qk(q, k, positions, cos, sin, rot_dim: int | None = None, layout: int = NEOX,

@@ -116,6 +116,13 @@ const char *ra_last_error(void) { return g_last_error; }
 
 ra_status rope_tables_build(float *cos_out, float *sin_out, int64_t rows, int rot_dim,
                             double base, int freq_dim, cudaStream_t s) {
+  return rope_tables_build_scaled(cos_out, sin_out, rows, rot_dim, base, freq_dim, 1.0, s);
+}
+
+ra_status rope_tables_build_scaled(float *cos_out, float *sin_out, int64_t rows, int rot_dim,
+                                   double base, int freq_dim, double pos_scale, cudaStream_t s) {
+  if (!(pos_scale > 0.0) || !isfinite(pos_scale))
+    return fail(RA_ERR_INVALID_ARG, "pos_scale must be finite and > 0");
   if (rows < 0) return fail(RA_ERR_INVALID_ARG, "rows must be >= 0 (got %lld)", (long long)rows);
   if (rot_dim < 2 || (rot_dim & 1))
     return fail(RA_ERR_INVALID_ARG, "rot_dim must be even and >= 2 (got %d)", rot_dim);
@@ -126,7 +133,7 @@ ra_status rope_tables_build(float *cos_out, float *sin_out, int64_t rows, int ro
   if (!aligned(cos_out, 4) || !aligned(sin_out, 4))
     return fail(RA_ERR_ALIGNMENT, "tables must be 4-byte aligned");
   if (rows == 0) return RA_OK;
-  const ra::TableArgs a{cos_out, sin_out, rows, rot_dim, freq_dim, base};
+  const ra::TableArgs a{cos_out, sin_out, rows, rot_dim, freq_dim, base, pos_scale};
   const cudaError_t e = ra::launch_table_build(a, s);
   return e == cudaSuccess ? RA_OK : cuda_fail(e, "rope_tables_build launch");
 }

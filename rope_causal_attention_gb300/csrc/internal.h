@@ -21,6 +21,7 @@ struct TableArgs {
   int64_t rows;
   int rot_dim, freq_dim;
   double base;
+  double pos_scale;  // angle = (p / pos_scale) * theta_i
 };
 
 struct RopeArgs {

@@ -29,14 +29,14 @@ namespace {
 // ------------------------------------------------------------------ tables
 __global__ void rope_table_build_kernel(float *__restrict__ cos_out,
                                         float *__restrict__ sin_out, int64_t rows, int half,
-                                        double base, int F) {
+                                        double base, int F, double pos_scale) {
   const int64_t n = rows * half;
   for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < n;
        idx += (int64_t)gridDim.x * blockDim.x) {
     const int64_t p = idx / half;
     const int i = (int)(idx - p * half);
     const double theta = pow(base, -(2.0 * i) / (double)F);
-    const double angle = (double)p * theta;
+    const double angle = ((double)p / pos_scale) * theta;  // p / 1.0 == p exactly
     double s, c;
     sincos(angle, &s, &c);
     cos_out[idx] = (float)c;
@@ -263,7 +263,7 @@ cudaError_t launch_table_build(const TableArgs &a, cudaStream_t s) {
   const int64_t cap = (int64_t)sm_count() * 32;
   if (blocks > cap) blocks = cap;
   rope_table_build_kernel<<<(unsigned)blocks, 256, 0, s>>>(a.cos_out, a.sin_out, a.rows, half,
-                                                          a.base, F);
+                                                          a.base, F, a.pos_scale);
   return cudaGetLastError();
 }
 

@@ -37,7 +37,7 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ["rope_tables_build", "rope_apply_qk", "attn_fwd_causal_rope",
+    for n in ["rope_tables_build", "rope_tables_build_scaled", "rope_apply_qk", "attn_fwd_causal_rope",
               "ra_get_device_status", "ra_status_string", "ra_last_error"]:
         assert n in names
 
@@ -88,6 +88,10 @@ def test_tables_rejections(L):
     assert L.rope_tables_build(None, s, 4, 8, 10000.0, 0, None) == INVALID
     assert L.rope_tables_build(p(2), s, 4, 8, 10000.0, 0, None) == ALIGN
     assert L.rope_tables_build(c, s, 0, 8, 10000.0, 0, None) == OK  # nothing to do
+    for bad in (0.0, -4.0, float("nan"), float("inf")):
+        assert L.rope_tables_build_scaled(c, s, 4, 8, 10000.0, 0, bad, None) == INVALID
+    assert L.rope_tables_build_scaled(c, s, 4, 7, 10000.0, 0, 4.0, None) == INVALID
+    assert L.rope_tables_build_scaled(c, s, 0, 8, 10000.0, 0, 4.0, None) == OK
 
 
 @no_gpu

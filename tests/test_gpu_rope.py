@@ -240,3 +240,30 @@ def test_continuous_batching_workload_full_size(ra, orc):
     idx = torch.from_numpy(sel)
     check_rotated(qg.cpu()[idx], q[idx], pos[sel], orc, W.rot_dim, W.base, W.layout)
     check_rotated(kg.cpu()[idx], k[idx], pos[sel], orc, W.rot_dim, W.base, W.layout)
+
+
+@pytest.mark.parametrize("scale,rows,rot_dim,base", [(1.0, 4096, 64, 10000.0), (4.0, 8192, 128, 10000.0),
+                                                    (1.5, 3000, 64, 500000.0)])
+def test_interpolated_tables_match_oracle(ra, orc, scale, rows, rot_dim, base):
+    """rope_tables_build_scaled (position interpolation) against the oracle,
+    same bound as the plain tables; a rotation through the scaled table equals
+    the oracle's rotation at fractional positions p / scale."""
+    c, s = ra.make_tables(rows, rot_dim, base, pos_scale=scale)
+    torch.cuda.synchronize()
+    wc, ws = orc.rope_tables_scaled(rows, rot_dim, base, scale)
+    for got, want in ((c, wc), (s, ws)):
+        g = got.cpu().double().numpy()
+        assert np.abs(g - want).max() <= 2.0 ** -24
+        assert (g == want.astype(np.float32).astype(np.float64)).mean() > 0.999
+    q, k = wl.rope_qk(16, 2, 1, rot_dim, torch.float32, seed=8)
+    pos = np.arange(0, rows, rows // 16)[:16]
+    qg, kg = q.cuda(), k.cuda()
+    ra.rope_apply_qk(qg, kg, torch.from_numpy(pos).cuda(), c, s)
+    xr = q.double().numpy()
+    want_q = np.empty_like(xr)
+    half = rot_dim // 2
+    for t in range(16):
+        lo, hi = xr[t, :, :half], xr[t, :, half:]
+        want_q[t, :, :half] = lo * wc[pos[t]] - hi * ws[pos[t]]
+        want_q[t, :, half:] = hi * wc[pos[t]] + lo * ws[pos[t]]
+    assert np.abs(qg.cpu().double().numpy() - want_q).max() <= 1e-5

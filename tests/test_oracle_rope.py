@@ -226,3 +226,31 @@ def test_rope_tokens_uses_token_positions(oracle_mod):
     for t in range(5):
         for h in range(3):
             assert np.array_equal(y[t, h], oracle_mod.rope_rows(x[t, h][None], [pos[t]])[0])
+
+
+def test_interpolated_tables_pins(oracle_mod):
+    """Position interpolation ("RoPE and FlashAttention ...", section 3): the
+    table at factor s holds the angles of positions p / s.  Factor 1 is the
+    plain table bit for bit; row k*s at factor s (s a power of two, so p / s is
+    exact) is row k of the plain table bit for bit; column 0 is cos(p / s)
+    (theta_0 = 1); scores of rotated pairs still depend only on the (scaled)
+    offset."""
+    c1, s1 = oracle_mod.rope_tables(64, 8, 10000.0)
+    cs, ss = oracle_mod.rope_tables_scaled(64, 8, 10000.0, 1.0)
+    assert np.array_equal(c1, cs) and np.array_equal(s1, ss)
+    c4, s4 = oracle_mod.rope_tables_scaled(256, 8, 10000.0, 4.0)
+    assert np.array_equal(c4[::4], c1) and np.array_equal(s4[::4], s1)
+    p = np.arange(256)
+    np.testing.assert_allclose(c4[:, 0], np.cos(p / 4.0), atol=1e-15)
+    c15, s15 = oracle_mod.rope_tables_scaled(300, 16, 500000.0, 1.5)
+    # angle addition across rows: row a+b from rows a and b (angles are linear in p)
+    for a, b in [(3, 7), (100, 150), (1, 298)]:
+        np.testing.assert_allclose(c15[a + b], c15[a] * c15[b] - s15[a] * s15[b], atol=1e-13)
+        np.testing.assert_allclose(s15[a + b], s15[a] * c15[b] + c15[a] * s15[b], atol=1e-13)
+    # a larger base is not position division: theta_0 = 1 under any base, so
+    # column 0 of a larger-base table is the plain column 0, while the
+    # interpolated table's column 0 turns at 1/s the rate
+    cb, _ = oracle_mod.rope_tables(64, 8, 40000.0)
+    assert np.array_equal(cb[:, 0], c1[:, 0])
+    assert not np.allclose(c4[:64, 0], c1[:, 0])
+    assert not np.allclose(cb[:, 1], c1[:, 1])
