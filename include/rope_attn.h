@@ -152,6 +152,94 @@ ra_status attn_fwd_causal_rope(const void *q, const void *k, const void *v, void
                                cudaStream_t s);
 
 /*
+ * Decoder KV cache ([RF] 2: new K is appended rotated, V unrotated, and cached
+ * K is never rotated again).  Row r of head h of the K cache starts at element
+ * k[r * k_strides[0] + h * k_strides[1]] (D contiguous elements; likewise V),
+ * r in [0, rows).  Cache sequence s owns the rows from seq_start[s] on: the
+ * key at position j of sequence s lives in row seq_start[s] + j.  Token-major
+ * ([rows][Hkv][D]), head-major ([Hkv][rows][D]) and interleaved K/V layouts
+ * are all expressible.  The caller owns every buffer and keeps each
+ * sequence's rows inside its own region.
+ *   k, v: device, dt.  seq_start: device int64 [n_seqs].
+ */
+typedef struct {
+  void *k;
+  void *v;
+  int64_t k_strides[2]; /* {row, head}, elements */
+  int64_t v_strides[2];
+  int64_t rows;
+  const int64_t *seq_start;
+  int64_t n_seqs;
+} ra_kv_cache;
+
+/*
+ * rope_append_kv -- the decoder step of [RF] 2 in one launch: rotate the new
+ * tokens' Q, rotate their K into the cache, copy their V into the cache.
+ *   Token t belongs to cache sequence s = seq_ids[t] (seq_ids NULL: s = t)
+ *   and sits at absolute position p = positions[t] (int32 or int64), its
+ *   cache row being seq_start[s] + p.  With Q, K rotated as in rope_apply_qk
+ *   (layout, rot_dim, tables):
+ *     q_out[t][h]                = rot(q[t][h], p)    h < Hq (in place if q_out is NULL or q)
+ *     cache.k[seq_start[s] + p][h] = rot(k_new[t][h], p)  all D dims (tail copied)
+ *     cache.v[seq_start[s] + p][h] = v_new[t][h]          h < Hkv
+ *   q [T][Hq][D], k_new / v_new [T][Hkv][D]: device, dt, strides {token,
+ *   head} in strides_q / strides_kn / strides_vn (q_out: strides_qo).  Hq may
+ *   be 0 (q NULL: cache append only).
+ *   A token whose s is outside [0, n_seqs), whose p is outside [0, table_rows)
+ *   or whose row is outside [0, cache.rows) is skipped (nothing of it is
+ *   written) and RA_ERR_POSITION_RANGE is recorded in the status word.
+ *   Rejected on the host: cache rows overlapping each other or an input
+ *   (RA_ERR_OVERLAP), q_out partly overlapping q.  Two tokens writing one
+ *   cache row is the caller's error (the result is one of them).
+ */
+ra_status rope_append_kv(void *q, void *q_out, const void *k_new, const void *v_new,
+                         const ra_kv_cache *cache, ra_dtype dt, int64_t T, int Hq, int Hkv, int D,
+                         int rot_dim, ra_layout layout, const int64_t strides_q[2],
+                         const int64_t strides_qo[2], const int64_t strides_kn[2],
+                         const int64_t strides_vn[2], const int32_t *seq_ids,
+                         const void *positions, int pos_is_int64, const float *cos_t,
+                         const float *sin_t, int64_t table_rows, cudaStream_t s);
+
+/*
+ * attn_decode_workspace_size -- bytes of device workspace attn_decode needs
+ * for these sizes on the current device (0: none).  Deterministic for fixed
+ * arguments and device; -1 cast to size_t for invalid sizes.
+ */
+size_t attn_decode_workspace_size(ra_dtype dt, int B, int Hq, int Hkv, int Sq, int D,
+                                  int64_t max_kv_len);
+
+/*
+ * attn_decode -- causal attention of Sq new queries per sequence over a KV
+ * cache that already holds rotated K ([RF] 2, 4, 5; the offset mask of [RF]
+ * 5).  Q must already be rotated (rope_append_kv); nothing is rotated here.
+ *   Batch entry b reads cache sequence s = seq_ids[b] (NULL: s = b) with
+ *   L = kv_len[b] keys at positions 0..L-1 (device int32 [B]); its query i
+ *   sits at position L - Sq + i and sees keys j <= L - Sq + i:
+ *     s_ij = softmax_scale * <q_i, k_j>, O_i = sum_j softmax(s_i)_j v_j,
+ *     LSE_i = m_i + ln(l_i) (natural log, scale included).
+ *   q-head h reads kv-head h / (Hq / Hkv).
+ *   q, o: device [B][Hq][Sq][D] of dt, strides {b, h, s} (token-major decode
+ *   batches are {Sq*Hq*D, D, Hq*D}); lse: device fp32 [B][Hq][Sq] or NULL.
+ *   The keys are split into chunks processed in parallel and merged by their
+ *   log-sum-exp (split-KV); the partial results live in `workspace` (device,
+ *   256-byte aligned, >= attn_decode_workspace_size bytes, contents ignored
+ *   on entry and clobbered).  Calls sharing a workspace must be ordered on
+ *   one stream.
+ *   max_kv_len >= max_b kv_len[b] (host value; it sizes the split).  An entry
+ *   with L < Sq, L > max_kv_len, s outside [0, n_seqs) or rows outside the
+ *   cache leaves its outputs unwritten and records RA_ERR_POSITION_RANGE.
+ *   bf16/fp16 with D = 128 and (Hq/Hkv)*Sq <= 64 run on the tensor cores
+ *   (tcgen05; K, V loaded by TMA: cache pointers 16-byte aligned, strides
+ *   multiples of 8 elements); every other case (fp32, D <= 256 even) runs a
+ *   CUDA-core kernel.  softmax_scale <= 0 selects 1/sqrt(D).
+ */
+ra_status attn_decode(const void *q, void *o, float *lse, const ra_kv_cache *cache, ra_dtype dt,
+                      int B, int Hq, int Hkv, int Sq, int D, const int32_t *seq_ids,
+                      const int32_t *kv_len, int64_t max_kv_len, float softmax_scale,
+                      const int64_t strides_q[3], const int64_t strides_o[3], void *workspace,
+                      size_t workspace_bytes, cudaStream_t s);
+
+/*
  * ra_get_device_status -- synchronise stream s, then read and clear the
  * current device's status word.  Returns RA_OK, the first error a kernel
  * recorded since the last call, or RA_ERR_CUDA if the stream reported an

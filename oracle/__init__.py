@@ -11,6 +11,8 @@ Contents
   library built from ``oracle.c`` (fp64, libm).
 * ``attention``: naive two-pass causal softmax attention with optional RoPE,
   for all rows or a selected subset (C, fp64, threaded over rows).
+* ``decode_attention``: the decoder step's attention over a KV cache of
+  already-rotated keys (per sequence, the same naive attention).
 * ``tiled_attention`` (``oracle.tiled``): the Q-block-outer / K-block-inner
   online-softmax recurrence, used only to show that the recurrence reaches
   the naive result.
@@ -185,4 +187,33 @@ def attention(q, k, v, kv_offset: int = 0, apply_rope: bool = True, rot_dim: int
         raise ValueError(f"invalid attention arguments (oracle rc={rc})")
     if full:
         return o.reshape(B, Hq, Sq, D), lse.reshape(B, Hq, Sq)
+    return o, lse
+
+
+def decode_attention(q, k_cache, v_cache, seq_start, kv_len, seq_ids=None,
+                     scale: float | None = None, nthreads: int | None = None):
+    """Attention of a decoder step over a KV cache, fp64 ("RoPE and
+    FlashAttention: relative positions and online softmax", section 2: the
+    cache holds rotated K and raw V, new queries are rotated before the
+    product; section 5: the offset causal mask).
+
+    q [B,Hq,Sq,D] holds the (already rotated) new queries; k_cache, v_cache
+    [rows, Hkv, D].  Entry b reads cache sequence s = seq_ids[b] (default b):
+    L = kv_len[b] keys at rows seq_start[s] + j, j < L; its query i sits at
+    position L - Sq + i and sees keys j <= L - Sq + i.  Nothing is rotated
+    here.  Returns O [B,Hq,Sq,D] and LSE [B,Hq,Sq] (natural log, scale
+    included)."""
+    q = np.asarray(q)
+    B, Hq, Sq, D = q.shape
+    o = np.empty((B, Hq, Sq, D), dtype=np.float64)
+    lse = np.empty((B, Hq, Sq), dtype=np.float64)
+    for b in range(B):
+        s = int(seq_ids[b]) if seq_ids is not None else b
+        L = int(kv_len[b])
+        r0 = int(seq_start[s])
+        kb = np.asarray(k_cache[r0:r0 + L]).transpose(1, 0, 2)[None]
+        vb = np.asarray(v_cache[r0:r0 + L]).transpose(1, 0, 2)[None]
+        ob, lb = attention(q[b:b + 1], kb, vb, kv_offset=L - Sq, apply_rope=False, scale=scale,
+                           nthreads=nthreads)
+        o[b], lse[b] = ob[0], lb[0]
     return o, lse

@@ -19,7 +19,8 @@ import threading
 import torch
 
 __all__ = ["NEOX", "GPTJ", "RAError", "rope_tables_build", "rope_tables_build_scaled",
-           "make_tables", "rope_apply_qk",
+           "make_tables", "rope_apply_qk", "KVCache", "rope_append_kv", "attn_decode",
+           "attn_decode_workspace_size",
            "attn_fwd_causal_rope", "ra_get_device_status", "ra_status_string", "library_path",
            "lib"]
 
@@ -33,6 +34,14 @@ _lock = threading.Lock()
 _lib = None
 
 _i64p = ctypes.POINTER(ctypes.c_int64)
+
+
+class KVCacheDesc(ctypes.Structure):
+    """ctypes mirror of ra_kv_cache."""
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("k_strides", ctypes.c_int64 * 2), ("v_strides", ctypes.c_int64 * 2),
+                ("rows", ctypes.c_int64), ("seq_start", ctypes.c_void_p),
+                ("n_seqs", ctypes.c_int64)]
 
 
 class RAError(RuntimeError):
@@ -68,6 +77,17 @@ def lib():
                                                i32, i64, i32, i32, i32, vp, vp, i64, f32,
                                                _i64p, _i64p, _i64p, _i64p, vp]
             L.attn_fwd_causal_rope.restype = i32
+            cp = ctypes.POINTER(KVCacheDesc)
+            i32p = ctypes.POINTER(ctypes.c_int32)
+            L.rope_append_kv.argtypes = [vp, vp, vp, vp, cp, i32, i64, i32, i32, i32, i32, i32,
+                                         _i64p, _i64p, _i64p, _i64p, vp, vp, i32, vp, vp, i64,
+                                         vp]
+            L.rope_append_kv.restype = i32
+            L.attn_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i64]
+            L.attn_decode_workspace_size.restype = ctypes.c_size_t
+            L.attn_decode.argtypes = [vp, vp, vp, cp, i32, i32, i32, i32, i32, i32, vp, vp, i64,
+                                      f32, _i64p, _i64p, vp, ctypes.c_size_t, vp]
+            L.attn_decode.restype = i32
             L.ra_get_device_status.argtypes = [vp]
             L.ra_get_device_status.restype = i32
             L.ra_status_string.argtypes = [i32]
@@ -230,6 +250,136 @@ def attn_fwd_causal_rope(q, k, v, cos=None, sin=None, kv_offset: int = 0, apply_
         int(kv_offset), int(bool(apply_rope)), rot_dim, int(layout), _ptr(cos), _ptr(sin), rows,
         float(softmax_scale) if softmax_scale is not None else 0.0, s3(q), s3(k), s3(v), s3(out),
         _stream(q.device, stream)), "attn_fwd_causal_rope")
+    return out, lse
+
+
+class KVCache:
+    """A decoder KV cache: k and v are [rows, Hkv, D] views (any strides with a
+    unit last stride; e.g. token-major tensors, or head-major storage
+    permuted to that shape), seq_start int64 [n_seqs] on the device holds each
+    sequence's first row; the key at position j of sequence s is row
+    seq_start[s] + j."""
+
+    def __init__(self, k: torch.Tensor, v: torch.Tensor, seq_start: torch.Tensor):
+        for t, n in ((k, "k"), (v, "v"), (seq_start, "seq_start")):
+            _cuda(t, n)
+        if k.dim() != 3 or v.shape != k.shape or k.dtype != v.dtype or k.dtype not in _DT:
+            raise ValueError("k and v must be [rows, Hkv, D] of one of fp32 / bf16 / fp16")
+        if k.stride(2) != 1 or v.stride(2) != 1:
+            raise ValueError("cache rows need a unit last stride")
+        if seq_start.dtype != torch.int64 or seq_start.dim() != 1 or not seq_start.is_contiguous():
+            raise ValueError("seq_start must be contiguous int64 [n_seqs]")
+        self.k, self.v, self.seq_start = k, v, seq_start
+
+    @property
+    def Hkv(self):
+        return self.k.shape[1]
+
+    @property
+    def D(self):
+        return self.k.shape[2]
+
+    def desc(self) -> KVCacheDesc:
+        d = KVCacheDesc()
+        d.k, d.v = self.k.data_ptr(), self.v.data_ptr()
+        d.k_strides[0], d.k_strides[1] = self.k.stride(0), self.k.stride(1)
+        d.v_strides[0], d.v_strides[1] = self.v.stride(0), self.v.stride(1)
+        d.rows = self.k.shape[0]
+        d.seq_start = self.seq_start.data_ptr()
+        d.n_seqs = self.seq_start.shape[0]
+        return d
+
+
+def rope_append_kv(cache: KVCache, q, k_new, v_new, positions, cos, sin, seq_ids=None,
+                   layout: int = NEOX, q_out=None, stream=None):
+    """Rotates q [T,Hq,D] (in place unless q_out), writes rot(k_new) and v_new
+    ([T,Hkv,D]) into the cache rows seq_start[seq_ids[t]] + positions[t]
+    (seq_ids None: token t is sequence t).  q may be None.  Returns q's result."""
+    for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new"), (positions, "positions"),
+                 (cos, "cos"), (sin, "sin"), (seq_ids, "seq_ids"), (q_out, "q_out")):
+        _cuda(t, n)
+    if k_new.dim() != 3 or v_new.shape != k_new.shape:
+        raise ValueError("k_new and v_new must be [T, Hkv, D]")
+    T, Hkv, D = k_new.shape
+    dt = cache.k.dtype
+    if k_new.dtype != dt or v_new.dtype != dt or (q is not None and q.dtype != dt):
+        raise ValueError("q, k_new, v_new must have the cache's dtype")
+    if Hkv != cache.Hkv or D != cache.D:
+        raise ValueError("k_new heads / head size must match the cache")
+    for t, n in ((q, "q"), (q_out, "q_out"), (k_new, "k_new"), (v_new, "v_new")):
+        if t is not None and (t.dim() != 3 or t.shape[0] != T or t.shape[2] != D
+                              or t.stride(2) != 1):
+            raise ValueError(f"{n} must be [T, H, D] with unit last stride")
+    if q_out is not None and (q is None or q_out.shape != q.shape or q_out.dtype != q.dtype):
+        raise ValueError("q_out must match q")
+    if positions.dtype not in (torch.int32, torch.int64) or positions.shape != (T,):
+        raise ValueError("positions must be int32 or int64 [T]")
+    if seq_ids is not None and (seq_ids.dtype != torch.int32 or seq_ids.shape != (T,)
+                                or not seq_ids.is_contiguous()):
+        raise ValueError("seq_ids must be contiguous int32 [T]")
+    if cos.dtype != torch.float32 or cos.shape != sin.shape or not cos.is_contiguous():
+        raise ValueError("tables must be contiguous fp32 of equal shape")
+    rot_dim = 2 * cos.shape[1]
+    Hq = q.shape[1] if q is not None else 0
+    st = lambda t: _arr([t.stride(0), t.stride(1)]) if t is not None else None
+    d = cache.desc()
+    _check(lib().rope_append_kv(
+        _ptr(q), _ptr(q_out), _ptr(k_new), _ptr(v_new), ctypes.byref(d), _DT[dt], T, Hq, Hkv, D,
+        rot_dim, int(layout), st(q), st(q_out), st(k_new), st(v_new), _ptr(seq_ids),
+        _ptr(positions), int(positions.dtype == torch.int64), _ptr(cos), _ptr(sin), cos.shape[0],
+        _stream(k_new.device, stream)), "rope_append_kv")
+    return q_out if q_out is not None else q
+
+
+def attn_decode_workspace_size(dtype, B: int, Hq: int, Hkv: int, Sq: int, D: int,
+                               max_kv_len: int) -> int:
+    """Workspace bytes attn_decode needs on the current device."""
+    n = lib().attn_decode_workspace_size(_DT[dtype], B, Hq, Hkv, Sq, D, int(max_kv_len))
+    if n == ctypes.c_size_t(-1).value:
+        raise ValueError("invalid decode sizes")
+    return int(n)
+
+
+def attn_decode(cache: KVCache, q, kv_len, max_kv_len: int, seq_ids=None,
+                softmax_scale: float | None = None, out=None, lse=None, return_lse: bool = True,
+                workspace=None, stream=None):
+    """Decode attention over the cache (rotated K, raw V).  q [B,Hq,Sq,D]
+    (already rotated; any strides with unit last stride), kv_len int32 [B]
+    keys of each entry (the Sq new ones included), max_kv_len >= max(kv_len).
+    Query i of entry b sits at kv_len[b] - Sq + i.  Returns (O, LSE or None)."""
+    for t, n in ((q, "q"), (kv_len, "kv_len"), (seq_ids, "seq_ids"), (out, "out"), (lse, "lse"),
+                 (workspace, "workspace")):
+        _cuda(t, n)
+    if q.dim() != 4 or q.stride(3) != 1:
+        raise ValueError("q must be [B, Hq, Sq, D] with unit last stride")
+    B, Hq, Sq, D = q.shape
+    if q.dtype != cache.k.dtype or D != cache.D:
+        raise ValueError("q must have the cache's dtype and head size")
+    if kv_len.dtype != torch.int32 or kv_len.shape != (B,) or not kv_len.is_contiguous():
+        raise ValueError("kv_len must be contiguous int32 [B]")
+    if seq_ids is not None and (seq_ids.dtype != torch.int32 or seq_ids.shape != (B,)
+                                or not seq_ids.is_contiguous()):
+        raise ValueError("seq_ids must be contiguous int32 [B]")
+    if out is None:
+        out = torch.empty((B, Hq, Sq, D), dtype=q.dtype, device=q.device)
+    elif out.shape != (B, Hq, Sq, D) or out.dtype != q.dtype or out.stride(3) != 1:
+        raise ValueError("out must be [B, Hq, Sq, D] in q's dtype with unit last stride")
+    if return_lse and lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    if lse is not None and (lse.shape != (B, Hq, Sq) or lse.dtype != torch.float32
+                            or not lse.is_contiguous()):
+        raise ValueError("lse must be contiguous fp32 [B, Hq, Sq]")
+    need = attn_decode_workspace_size(q.dtype, B, Hq, cache.Hkv, Sq, D, max_kv_len)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    s3 = lambda t: _arr([t.stride(0), t.stride(1), t.stride(2)])
+    d = cache.desc()
+    _check(lib().attn_decode(
+        _ptr(q), _ptr(out), _ptr(lse), ctypes.byref(d), _DT[q.dtype], B, Hq, cache.Hkv, Sq, D,
+        _ptr(seq_ids), _ptr(kv_len), int(max_kv_len),
+        float(softmax_scale) if softmax_scale is not None else 0.0, s3(q), s3(out),
+        _ptr(workspace), wbytes, _stream(q.device, stream)), "attn_decode")
     return out, lse
 
 

@@ -8,6 +8,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "internal.h"
@@ -88,9 +89,64 @@ int *device_status_ptr(cudaError_t *err) {
   return g_status_ptr[dev];
 }
 
+int sm_count_current() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+    return 148;
+  return n;
+}
+
 }  // namespace ra
 
 using ra::fail;
+
+namespace {
+
+// True when the rows of a [n0][n1][D] strided array share no byte (strides
+// in elements): taken in increasing stride order, each dimension of size > 1
+// steps past everything the smaller ones cover.
+bool rows_distinct(int64_t n0, int64_t s0, int64_t n1, int64_t s1, int64_t D) {
+  int64_t n[2] = {n0, n1}, st[2] = {s0, s1};
+  if (st[0] > st[1]) {
+    std::swap(n[0], n[1]);
+    std::swap(st[0], st[1]);
+  }
+  int64_t ext = D;
+  for (int j = 0; j < 2; ++j) {
+    if (n[j] <= 1) continue;
+    if (st[j] < ext) return false;
+    ext = (n[j] - 1) * st[j] + ext;
+  }
+  return true;
+}
+
+int64_t span4(int64_t n0, int64_t s0, int64_t n1, int64_t s1, int64_t n2, int64_t s2, int64_t D,
+              size_t es) {
+  return ((n0 - 1) * s0 + (n1 - 1) * s1 + (n2 - 1) * s2 + D) * (int64_t)es;
+}
+
+bool spans_apart(const void *a, int64_t na, const void *b, int64_t nb) {
+  const char *x = static_cast<const char *>(a), *y = static_cast<const char *>(b);
+  return x + na <= y || y + nb <= x;
+}
+
+// Host checks shared by the two cache calls; nullptr when the cache is valid.
+const char *cache_problem(const ra_kv_cache *c, int Hkv, int D, size_t es) {
+  if (!c) return "cache must be non-NULL";
+  if (!c->k || !c->v || !c->seq_start) return "cache k, v and seq_start must be non-NULL";
+  if (c->rows < 1 || c->n_seqs < 1) return "cache rows and n_seqs must be >= 1";
+  for (int j = 0; j < 2; ++j)
+    if (c->k_strides[j] < 0 || c->v_strides[j] < 0) return "cache strides must be >= 0";
+  if (!rows_distinct(c->rows, c->k_strides[0], Hkv, c->k_strides[1], D) ||
+      !rows_distinct(c->rows, c->v_strides[0], Hkv, c->v_strides[1], D))
+    return "cache strides make two rows share memory";
+  if (!aligned(c->k, es) || !aligned(c->v, es) || !aligned(c->seq_start, 8))
+    return "cache buffers misaligned";
+  return nullptr;
+}
+
+}  // namespace
 
 static ra_status cuda_fail(cudaError_t e, const char *what) {
   return fail(RA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
@@ -320,6 +376,176 @@ ra_status attn_fwd_causal_rope(const void *q, const void *k, const void *v, void
   e = ra::launch_attn_tc(a, s);
   if (e == cudaErrorNotSupported) return fail(RA_ERR_UNSUPPORTED, "no tensor-core variant");
   return e == cudaSuccess ? RA_OK : cuda_fail(e, "attention (tensor core) launch");
+}
+
+ra_status rope_append_kv(void *q, void *q_out, const void *k_new, const void *v_new,
+                         const ra_kv_cache *cache, ra_dtype dt, int64_t T, int Hq, int Hkv, int D,
+                         int rot_dim, ra_layout layout, const int64_t strides_q[2],
+                         const int64_t strides_qo[2], const int64_t strides_kn[2],
+                         const int64_t strides_vn[2], const int32_t *seq_ids,
+                         const void *positions, int pos_is_int64, const float *cos_t,
+                         const float *sin_t, int64_t table_rows, cudaStream_t s) {
+  if (!dtype_ok(dt)) return fail(RA_ERR_INVALID_ARG, "unknown dtype %d", (int)dt);
+  if (!layout_ok(layout)) return fail(RA_ERR_INVALID_ARG, "unknown layout %d", (int)layout);
+  if (T < 0 || Hq < 0 || Hkv < 1) return fail(RA_ERR_INVALID_ARG, "need T >= 0, Hq >= 0, Hkv >= 1");
+  if (D < 2 || (D & 1)) return fail(RA_ERR_INVALID_ARG, "D must be even and >= 2 (got %d)", D);
+  if (rot_dim < 2 || (rot_dim & 1) || rot_dim > D)
+    return fail(RA_ERR_INVALID_ARG, "rot_dim must be even with 2 <= rot_dim <= D (got %d)", rot_dim);
+  if ((Hq > 0) != (q != nullptr)) return fail(RA_ERR_INVALID_ARG, "q must be non-NULL exactly when Hq > 0");
+  if (!k_new || !v_new) return fail(RA_ERR_INVALID_ARG, "k_new and v_new must be non-NULL");
+  const size_t es = dtype_size(dt);
+  if (const char *why = cache_problem(cache, Hkv, D, es)) return fail(RA_ERR_INVALID_ARG, "%s", why);
+  if (table_rows < 1) return fail(RA_ERR_INVALID_ARG, "table_rows must be >= 1");
+  if (!positions || !cos_t || !sin_t)
+    return fail(RA_ERR_INVALID_ARG, "positions and tables must be non-NULL");
+  const bool qin = q_out == nullptr || q_out == q;
+  if (!strides_kn || !strides_vn || (Hq > 0 && !strides_q) || (Hq > 0 && !qin && !strides_qo))
+    return fail(RA_ERR_INVALID_ARG, "stride arrays must be non-NULL for every tensor used");
+  const int64_t zero2[2] = {0, 0};
+  const int64_t *sq = Hq > 0 ? strides_q : zero2;
+  const int64_t *sqo = (Hq > 0 && !qin) ? strides_qo : sq;
+  for (int j = 0; j < 2; ++j)
+    if (sq[j] < 0 || sqo[j] < 0 || strides_kn[j] < 0 || strides_vn[j] < 0)
+      return fail(RA_ERR_INVALID_ARG, "strides must be >= 0");
+  if (T == 0) return RA_OK;
+
+  // overlap: the written regions (q_out or q, cache K, cache V) share no byte
+  // with each other or with the inputs; q_out may equal q
+  const Region rkn = region(k_new, T, strides_kn[0], Hkv, strides_kn[1], D, es);
+  const Region rvn = region(v_new, T, strides_vn[0], Hkv, strides_vn[1], D, es);
+  const Region rkc = region(cache->k, cache->rows, cache->k_strides[0], Hkv, cache->k_strides[1], D, es);
+  const Region rvc = region(cache->v, cache->rows, cache->v_strides[0], Hkv, cache->v_strides[1], D, es);
+  if (!disjoint(rkc, rvc)) return fail(RA_ERR_OVERLAP, "cache K and V rows overlap");
+  for (const Region *r : {&rkn, &rvn})
+    if (!disjoint(rkc, *r) || !disjoint(rvc, *r))
+      return fail(RA_ERR_OVERLAP, "the cache overlaps k_new or v_new");
+  if (Hq > 0) {
+    const Region rq = region(q, T, sq[0], Hq, sq[1], D, es);
+    const Region rqo = region(qin ? q : q_out, T, sqo[0], Hq, sqo[1], D, es);
+    for (const Region *w : {&rq, &rqo})
+      for (const Region *r : {&rkn, &rvn, &rkc, &rvc})
+        if (!disjoint(*w, *r)) return fail(RA_ERR_OVERLAP, "q or q_out overlaps k, v or the cache");
+    if (!qin && !disjoint(rq, rqo)) return fail(RA_ERR_OVERLAP, "q_out partially overlaps q");
+  }
+
+  if (!aligned(positions, pos_is_int64 ? 8 : 4) || !aligned(cos_t, 4) || !aligned(sin_t, 4) ||
+      (seq_ids && !aligned(seq_ids, 4)))
+    return fail(RA_ERR_ALIGNMENT, "positions, seq_ids or tables misaligned");
+  const void *ptrs[6] = {q, qin ? q : q_out, k_new, v_new, cache->k, cache->v};
+  for (const void *p : ptrs)
+    if (p && !aligned(p, es)) return fail(RA_ERR_ALIGNMENT, "buffers must be element-aligned");
+
+  // vector path: 16-byte aligned pointers and strides, whole 16-byte slices
+  const int V = (int)(16 / es);
+  const int half = rot_dim / 2;
+  bool vec = aligned(cos_t, 16) && aligned(sin_t, 16);
+  for (const void *p : ptrs) vec = vec && (!p || aligned(p, 16));
+  for (int j = 0; j < 2; ++j)
+    vec = vec && sq[j] % V == 0 && sqo[j] % V == 0 && strides_kn[j] % V == 0 &&
+          strides_vn[j] % V == 0 && cache->k_strides[j] % V == 0 && cache->v_strides[j] % V == 0;
+  vec = vec && (layout == RA_NEOX ? half % V == 0 : rot_dim % V == 0) && (D - rot_dim) % V == 0;
+
+  cudaError_t e;
+  int *status = ra::device_status_ptr(&e);
+  if (!status) return cuda_fail(e, "status word");
+  ra::AppendArgs a{};
+  a.q = q; a.q_out = q_out; a.k_new = k_new; a.v_new = v_new; a.cache = *cache; a.dt = dt;
+  a.T = T; a.Hq = Hq; a.Hkv = Hkv; a.D = D; a.rot_dim = rot_dim; a.layout = layout;
+  for (int j = 0; j < 2; ++j) {
+    a.sq[j] = sq[j]; a.sqo[j] = sqo[j]; a.skn[j] = strides_kn[j]; a.svn[j] = strides_vn[j];
+  }
+  a.seq_ids = seq_ids; a.positions = positions; a.pos_is_int64 = pos_is_int64 ? 1 : 0;
+  a.cos_t = cos_t; a.sin_t = sin_t; a.table_rows = table_rows; a.status = status;
+  e = ra::launch_rope_append(a, vec, s);
+  return e == cudaSuccess ? RA_OK : cuda_fail(e, "rope_append_kv launch");
+}
+
+size_t attn_decode_workspace_size(ra_dtype dt, int B, int Hq, int Hkv, int Sq, int D,
+                                  int64_t max_kv_len) {
+  ra::DecodePlan plan;
+  if (!dtype_ok(dt) || !ra::plan_decode(dt, B, Hq, Hkv, Sq, D, max_kv_len, &plan))
+    return (size_t)-1;
+  return plan.ws_bytes;
+}
+
+ra_status attn_decode(const void *q, void *o, float *lse, const ra_kv_cache *cache, ra_dtype dt,
+                      int B, int Hq, int Hkv, int Sq, int D, const int32_t *seq_ids,
+                      const int32_t *kv_len, int64_t max_kv_len, float softmax_scale,
+                      const int64_t strides_q[3], const int64_t strides_o[3], void *workspace,
+                      size_t workspace_bytes, cudaStream_t s) {
+  if (!dtype_ok(dt)) return fail(RA_ERR_INVALID_ARG, "unknown dtype %d", (int)dt);
+  if (B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv)
+    return fail(RA_ERR_INVALID_ARG, "need B >= 0, Hq and Hkv >= 1, Hq a multiple of Hkv");
+  if (Sq < 1) return fail(RA_ERR_INVALID_ARG, "Sq must be >= 1");
+  if (D < 2 || (D & 1) || D > 256)
+    return fail(RA_ERR_INVALID_ARG, "D must be even with 2 <= D <= 256 (got %d)", D);
+  if (max_kv_len < Sq) return fail(RA_ERR_INVALID_ARG, "max_kv_len must be >= Sq");
+  if (!(softmax_scale <= 0.f) && !isfinite(softmax_scale))
+    return fail(RA_ERR_INVALID_ARG, "softmax_scale must be finite");
+  if (!q || !o || !kv_len) return fail(RA_ERR_INVALID_ARG, "q, o and kv_len must be non-NULL");
+  if (!strides_q || !strides_o) return fail(RA_ERR_INVALID_ARG, "stride arrays must be non-NULL");
+  for (int j = 0; j < 3; ++j)
+    if (strides_q[j] < 0 || strides_o[j] < 0) return fail(RA_ERR_INVALID_ARG, "strides must be >= 0");
+  const size_t es = dtype_size(dt);
+  if (const char *why = cache_problem(cache, Hkv, D, es)) return fail(RA_ERR_INVALID_ARG, "%s", why);
+  ra::DecodePlan plan;
+  if (!ra::plan_decode(dt, B, Hq, Hkv, Sq, D, max_kv_len, &plan))
+    return fail(RA_ERR_INVALID_ARG, "sizes out of range for the split plan");
+  if (plan.ws_bytes > 0) {
+    if (!workspace) return fail(RA_ERR_INVALID_ARG, "workspace required (%zu bytes)", plan.ws_bytes);
+    if (workspace_bytes < plan.ws_bytes)
+      return fail(RA_ERR_INVALID_ARG, "workspace of %zu bytes < %zu required", workspace_bytes,
+                  plan.ws_bytes);
+    if (!aligned(workspace, 256)) return fail(RA_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  }
+  if (B == 0) return RA_OK;
+  if (!aligned(q, es) || !aligned(o, es) || (lse && !aligned(lse, 4)) || !aligned(kv_len, 4) ||
+      (seq_ids && !aligned(seq_ids, 4)))
+    return fail(RA_ERR_ALIGNMENT, "buffers must be element-aligned");
+  // written: o, lse, workspace; read: q, cache K and V
+  {
+    const int64_t qspan = span4(B, strides_q[0], Hq, strides_q[1], Sq, strides_q[2], D, es);
+    const int64_t ospan = span4(B, strides_o[0], Hq, strides_o[1], Sq, strides_o[2], D, es);
+    const int64_t kspan = span4(cache->rows, cache->k_strides[0], Hkv, cache->k_strides[1], 1, 0, D, es);
+    const int64_t vspan = span4(cache->rows, cache->v_strides[0], Hkv, cache->v_strides[1], 1, 0, D, es);
+    const int64_t lspan = (int64_t)B * Hq * Sq * 4;
+    const int64_t wspan = (int64_t)plan.ws_bytes;
+    struct { const void *p; int64_t n; } rd[3] = {{q, qspan}, {cache->k, kspan}, {cache->v, vspan}};
+    struct { const void *p; int64_t n; } wr[3] = {{o, ospan}, {lse, lse ? lspan : 0},
+                                                  {workspace, workspace ? wspan : 0}};
+    for (int w = 0; w < 3; ++w) {
+      if (!wr[w].p || wr[w].n == 0) continue;
+      for (int r = 0; r < 3; ++r)
+        if (!spans_apart(wr[w].p, wr[w].n, rd[r].p, rd[r].n))
+          return fail(RA_ERR_OVERLAP, "an output or the workspace overlaps q or the cache");
+      for (int w2 = w + 1; w2 < 3; ++w2)
+        if (wr[w2].p && wr[w2].n && !spans_apart(wr[w].p, wr[w].n, wr[w2].p, wr[w2].n))
+          return fail(RA_ERR_OVERLAP, "o, lse and the workspace must not overlap");
+    }
+  }
+  // the tensor-core kernel loads K and V with TMA and Q / stores O in 16-byte pieces
+  if (plan.tc) {
+    bool ok = aligned(cache->k, 16) && aligned(cache->v, 16) && aligned(q, 16) && aligned(o, 16);
+    for (int j = 0; j < 2; ++j) ok = ok && cache->k_strides[j] % 8 == 0 && cache->v_strides[j] % 8 == 0;
+    for (int j = 0; j < 3; ++j) ok = ok && strides_q[j] % 8 == 0 && strides_o[j] % 8 == 0;
+    plan.tc = ok;  // same split plan on the CUDA-core kernel otherwise
+  }
+
+  cudaError_t e;
+  ra::DecodeArgs a{};
+  a.status = ra::device_status_ptr(&e);
+  if (!a.status) return cuda_fail(e, "status word");
+  a.q = q; a.o = o; a.lse = lse; a.cache = *cache; a.dt = dt;
+  a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.Sq = Sq; a.D = D;
+  a.seq_ids = seq_ids; a.kv_len = kv_len; a.max_kv_len = max_kv_len;
+  a.scale = softmax_scale > 0.f ? softmax_scale : (float)(1.0 / sqrt((double)D));
+  for (int j = 0; j < 3; ++j) {
+    a.sq[j] = strides_q[j]; a.so[j] = strides_o[j];
+  }
+  a.workspace = workspace; a.plan = plan;
+  e = ra::launch_attn_decode(a, s);
+  if (e == cudaErrorNotSupported) return fail(RA_ERR_UNSUPPORTED, "no decode kernel for the case");
+  return e == cudaSuccess ? RA_OK : cuda_fail(e, "attn_decode launch");
 }
 
 ra_status ra_get_device_status(cudaStream_t s) {

@@ -32,4 +32,38 @@ __device__ __forceinline__ int64_t load_position(const void *positions, int is64
               : static_cast<int64_t>(static_cast<const int32_t *>(positions)[t]);
 }
 
+// 16-byte vector access: VecN<T>::N elements per uint4.
+template <typename T> struct VecN { static constexpr int N = 16 / (int)sizeof(T); };
+
+template <typename T>
+__device__ __forceinline__ void unpack16(const uint4 &u, float *f) {
+  const T *e = reinterpret_cast<const T *>(&u);
+#pragma unroll
+  for (int i = 0; i < VecN<T>::N; ++i) f[i] = Elem<T>::load(e[i]);
+}
+
+template <typename T>
+__device__ __forceinline__ uint4 pack16(const float *f) {
+  uint4 u;
+  T *e = reinterpret_cast<T *>(&u);
+#pragma unroll
+  for (int i = 0; i < VecN<T>::N; ++i) e[i] = Elem<T>::store(f[i]);
+  return u;
+}
+
+// Loads n consecutive fp32 table values (n = 2, 4 or 8) starting at p.
+template <int n>
+__device__ __forceinline__ void load_table(const float *__restrict__ p, float *out) {
+  if constexpr (n == 2) {
+    const float2 a = __ldg(reinterpret_cast<const float2 *>(p));
+    out[0] = a.x; out[1] = a.y;
+  } else {
+#pragma unroll
+    for (int j = 0; j < n / 4; ++j) {
+      const float4 a = __ldg(reinterpret_cast<const float4 *>(p) + j);
+      out[4 * j] = a.x; out[4 * j + 1] = a.y; out[4 * j + 2] = a.z; out[4 * j + 3] = a.w;
+    }
+  }
+}
+
 }  // namespace ra

@@ -56,7 +56,60 @@ struct AttnArgs {
   int *status;
 };
 
+struct AppendArgs {
+  void *q, *q_out;
+  const void *k_new, *v_new;
+  ra_kv_cache cache;
+  ra_dtype dt;
+  int64_t T;
+  int Hq, Hkv, D, rot_dim;
+  ra_layout layout;
+  int64_t sq[2], sqo[2], skn[2], svn[2];
+  const int32_t *seq_ids;
+  const void *positions;
+  int pos_is_int64;
+  const float *cos_t, *sin_t;
+  int64_t table_rows;
+  int *status;
+};
+
+// Split-KV plan of one decode call: keys of a sequence are cut into `splits`
+// chunks of `chunk` keys (a multiple of 128); splits == 1 writes O directly.
+struct DecodePlan {
+  bool tc;          // tensor-core kernel (else CUDA cores)
+  int splits;
+  int64_t chunk;
+  size_t ws_bytes;  // 0 when splits == 1
+  size_t ws_lse_offset;
+};
+// Returns false for invalid sizes.
+bool plan_decode(ra_dtype dt, int B, int Hq, int Hkv, int Sq, int D, int64_t max_kv_len,
+                 DecodePlan *plan);
+
+struct DecodeArgs {
+  const void *q;
+  void *o;
+  float *lse;
+  ra_kv_cache cache;
+  ra_dtype dt;
+  int B, Hq, Hkv, Sq, D;
+  const int32_t *seq_ids, *kv_len;
+  int64_t max_kv_len;
+  float scale;
+  int64_t sq[3], so[3];
+  void *workspace;
+  DecodePlan plan;
+  int *status;
+};
+
 cudaError_t launch_table_build(const TableArgs &a, cudaStream_t s);
+cudaError_t launch_rope_append(const AppendArgs &a, bool vectorized, cudaStream_t s);
+// Runs the split kernel (tensor-core or CUDA-core, as planned) and the merge.
+cudaError_t launch_attn_decode(const DecodeArgs &a, cudaStream_t s);
+// Tensor-core split kernel only (decode_tc.cu); cudaErrorNotSupported when it
+// has no variant for the case.
+cudaError_t launch_attn_decode_tc(const DecodeArgs &a, cudaStream_t s);
+int sm_count_current();
 cudaError_t launch_rope_apply(const RopeArgs &a, bool vectorized, cudaStream_t s);
 cudaError_t launch_attn_simt(const AttnArgs &a, cudaStream_t s);
 // Returns cudaErrorNotSupported when the tensor-core kernel has no variant

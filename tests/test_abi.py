@@ -37,7 +37,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ["rope_tables_build", "rope_tables_build_scaled", "rope_apply_qk", "attn_fwd_causal_rope",
+    for n in ["rope_tables_build", "rope_tables_build_scaled", "rope_apply_qk", "rope_append_kv",
+              "attn_decode", "attn_decode_workspace_size", "attn_fwd_causal_rope",
               "ra_get_device_status", "ra_status_string", "ra_last_error"]:
         assert n in names
 
@@ -147,3 +148,97 @@ def test_attention_rejections(L):
     assert attn(L, o=p(8)) == OVERLAP                     # output on top of q
     assert attn(L, q=p(2)) == ALIGN
     assert attn(L, strides=(4 * 8 * 64, 8 * 64, 60)) == ALIGN  # row stride not multiple of 8
+
+
+def kvc(k=A + (1 << 27), v=A + (1 << 28), ks=(16, 8), vs=(16, 8), rows=64, st=A + (1 << 29),
+        n=4):
+    from rope_causal_attention_gb300 import KVCacheDesc
+    c = KVCacheDesc()
+    c.k, c.v = k, v
+    c.k_strides[0], c.k_strides[1] = ks
+    c.v_strides[0], c.v_strides[1] = vs
+    c.rows, c.seq_start, c.n_seqs = rows, st, n
+    return c
+
+
+def append(L, cache=None, q=p(0), qo=None, kn=p(1 << 22), vn=p(1 << 23), dt=1, T=4, Hq=2,
+           Hkv=2, D=8, rot=8, lay=0, sq=(16, 8), sqo=None, skn=(16, 8), svn=(16, 8), ids=None,
+           pos=p(1 << 24), is64=0, rows=16):
+    c = kvc() if cache is None else cache
+    return L.rope_append_kv(q, qo, kn, vn, ctypes.byref(c) if c is not False else None, dt, T,
+                            Hq, Hkv, D, rot, lay, i64(*sq) if sq else None,
+                            i64(*sqo) if sqo else None, i64(*skn) if skn else None,
+                            i64(*svn) if svn else None, ids, pos, is64, p(1 << 25), p(1 << 26),
+                            rows, None)
+
+
+def test_decode_workspace_size(L):
+    L.attn_decode_workspace_size.restype = ctypes.c_size_t
+    bad = ctypes.c_size_t(-1).value
+    assert L.attn_decode_workspace_size(1, 1, 8, 8, 1, 128, 100) == 0       # one chunk
+    assert L.attn_decode_workspace_size(1, 1, 8, 3, 1, 128, 100) == bad     # Hq % Hkv
+    assert L.attn_decode_workspace_size(1, 1, 8, 8, 0, 128, 100) == bad     # Sq
+    assert L.attn_decode_workspace_size(1, 1, 8, 8, 1, 258, 100) == bad     # D > 256
+    assert L.attn_decode_workspace_size(9, 1, 8, 8, 1, 128, 100) == bad     # dtype
+    # long keys split into chunks: O partials (fp32 D per chunk) + one LSE per chunk
+    n = L.attn_decode_workspace_size(1, 4, 64, 8, 1, 128, 131072)
+    assert n != bad and n > 4 * 64 * 2 * 128 * 4
+
+
+@no_gpu
+def test_append_rejections(L):
+    assert append(L, cache=False) == INVALID
+    assert append(L, cache=kvc(k=0)) == INVALID
+    assert append(L, cache=kvc(rows=0)) == INVALID
+    assert append(L, cache=kvc(n=0)) == INVALID
+    assert append(L, cache=kvc(ks=(4, 8))) == INVALID     # rows of the K cache overlap
+    assert append(L, Hkv=0) == INVALID
+    assert append(L, D=7, rot=6) == INVALID
+    assert append(L, rot=10) == INVALID
+    assert append(L, q=None) == INVALID                    # Hq > 0 without q
+    assert append(L, kn=None) == INVALID
+    assert append(L, pos=None) == INVALID
+    assert append(L, rows=0) == INVALID
+    assert append(L, skn=None) == INVALID
+    assert append(L, sq=(-16, 8)) == INVALID
+    assert append(L, T=0) == OK                            # nothing to do
+    # cache V on top of cache K
+    assert append(L, cache=kvc(v=A + (1 << 27) + 8)) == OVERLAP
+    # cache K on top of k_new
+    assert append(L, cache=kvc(k=A + (1 << 22))) == OVERLAP
+    # q_out partially overlapping q
+    assert append(L, qo=p(2), sqo=(16, 8)) == OVERLAP
+    assert append(L, q=p(1)) == ALIGN
+    assert append(L, pos=p((1 << 24) + 4), is64=1) == ALIGN
+
+
+def decode(L, cache=None, q=p(0), o=p(1 << 22), lse=None, dt=1, B=2, Hq=4, Hkv=2, Sq=1, D=8,
+           ids=None, kvl=p(1 << 24), maxl=32, sq=(32, 8, 32), so=(32, 8, 32), ws=None, wsb=0):
+    c = kvc() if cache is None else cache
+    return L.attn_decode(q, o, lse, ctypes.byref(c) if c is not False else None, dt, B, Hq, Hkv,
+                         Sq, D, ids, kvl, maxl, ctypes.c_float(0.0), i64(*sq) if sq else None,
+                         i64(*so) if so else None, ws, ctypes.c_size_t(wsb), None)
+
+
+@no_gpu
+def test_decode_rejections(L):
+    assert decode(L, Hq=3) == INVALID                      # Hq % Hkv
+    assert decode(L, Sq=0) == INVALID
+    assert decode(L, D=7) == INVALID
+    assert decode(L, D=258) == INVALID
+    assert decode(L, maxl=0) == INVALID
+    assert decode(L, Sq=4, maxl=3) == INVALID              # max_kv_len < Sq
+    assert decode(L, q=None) == INVALID
+    assert decode(L, kvl=None) == INVALID
+    assert decode(L, cache=False) == INVALID
+    assert decode(L, sq=None) == INVALID
+    assert decode(L, dt=5) == INVALID
+    assert decode(L, B=0) == OK                            # nothing to do
+    # a long cache needs a workspace
+    assert decode(L, maxl=100000) == INVALID
+    assert decode(L, maxl=100000, ws=p(1 << 30), wsb=16) == INVALID   # too small
+    need = L.attn_decode_workspace_size(1, 2, 4, 2, 1, 8, 100000)
+    assert decode(L, maxl=100000, ws=ctypes.c_void_p(A + (1 << 30) + 8), wsb=need) == ALIGN
+    assert decode(L, o=p(8)) == OVERLAP                    # output on top of q
+    assert decode(L, o=ctypes.c_void_p(A + (1 << 27))) == OVERLAP      # output on the cache
+    assert decode(L, q=p(1)) == ALIGN

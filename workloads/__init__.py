@@ -45,6 +45,15 @@ def rope_qk(T, Hq, Hkv, D, dtype=torch.bfloat16, seed=0):
     return q, k
 
 
+def decode_tokens(T, Hq, Hkv, D, dtype=torch.bfloat16, seed=0):
+    """Token-major new-token q [T,Hq,D], k and v [T,Hkv,D], CPU, drawn in that order."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    q = randn((T, Hq, D), g, dtype)
+    k = randn((T, Hkv, D), g, dtype)
+    v = randn((T, Hkv, D), g, dtype)
+    return q, k, v
+
+
 def request_lengths(n_req: int, total: int, max_len: int, rng: np.random.Generator):
     """Lengths drawn uniform in [1, max_len], then moved by +-1 on randomly
     chosen requests (kept within [1, max_len]) until they sum to ``total``."""
