@@ -7,7 +7,10 @@ workload (bf16, B=1, 32 q-heads / 8 kv-heads, 16384 new queries after a
 4096-row cached prefix, D=128, NeoX, base 5e5): the largest single-GPU
 configuration of the attention metric.  The same run also times the
 standalone rope_apply_qk on the continuous-batching workload (bf16, 65536
-tokens of 256 requests, 32 + 8 heads, D=128, in place) and reports its GB/s.
+tokens of 256 requests, 32 + 8 heads, D=128, in place) and reports its GB/s,
+and the decoder step on the decode workload (512 requests, contexts up to
+131072 keys, ~140 GB of cached bf16 K/V): rope_append_kv plus attn_decode,
+reported as GB/s of the decode attention (object "decode_step").
 
 Timing: W untimed warm-up steps, then K steps, each timed with CUDA events on
 the launching stream; L2 is flushed (a 256 MiB write) before every timed
@@ -42,8 +45,10 @@ import workloads as wl  # noqa: E402
 METRIC = "fused RoPE causal attn TFLOPS (% bf16 peak); rope_apply GB/s (% HBM), 1 GB300"
 ATTN = wl.LONG_GQA
 ROPE = wl.CB_ROPE
+DEC = wl.DECODE_ATTN
 ATTN_KERNEL_SRC = os.path.join(ROOT, "rope_causal_attention_gb300", "csrc", "attn_tc.cu")
 ROPE_KERNEL_SRC = os.path.join(ROOT, "rope_causal_attention_gb300", "csrc", "rope_kernels.cu")
+DECODE_KERNEL_SRC = os.path.join(ROOT, "rope_causal_attention_gb300", "csrc", "decode_tc.cu")
 PROFILE_JSON = os.path.join(ROOT, "profiles", "counters.json")
 
 
@@ -303,6 +308,107 @@ def time_rope(ra, args, dev, stream):
     return {"ms": ms, "bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9, "T": T}
 
 
+def time_decode(ra, args, dev, stream, host_e2e=True):
+    """Times the decoder step on the decode workload: rope_append_kv of the
+    512 new tokens (Q rotated in place, rotated K and raw V written to the
+    cache) and attn_decode over each request's whole context.  The cache is
+    packed token-major ([rows][8][128], request b from row sum of the earlier
+    lengths) and filled on the device from a seeded generator; its ~140 GB
+    exceed L2, so no flush is needed."""
+    lens = DEC.kv_lens()
+    if args.decode_reqs:
+        lens = lens[:args.decode_reqs]
+    B = lens.shape[0]
+    dt = wl.DTYPES[DEC.dtype]
+    starts = np.concatenate([[0], np.cumsum(lens)[:-1]]).astype(np.int64)
+    rows = int(lens.sum())
+    g = torch.Generator(device=dev)
+    g.manual_seed(DEC.seed)
+    kc = torch.randn((rows, DEC.Hkv, DEC.D), generator=g, device=dev, dtype=dt)
+    vc = torch.randn((rows, DEC.Hkv, DEC.D), generator=g, device=dev, dtype=dt)
+    cache = ra.KVCache(kc, vc, torch.from_numpy(starts).to(dev))
+    q, kn, vn = DEC.new_tokens()
+    q, kn, vn = q[:B], kn[:B], vn[:B]
+    qg, kg, vg = q.to(dev), kn.to(dev), vn.to(dev)
+    pos = torch.from_numpy(lens - 1).to(torch.int32).to(dev)
+    kv_len = torch.from_numpy(lens).to(torch.int32).to(dev)
+    max_len = int(lens.max())
+    cos, sin = ra.make_tables(DEC.table_rows, DEC.rot_dim, DEC.base, device=dev)
+    wsb = ra.attn_decode_workspace_size(dt, B, DEC.Hq, DEC.Hkv, DEC.Sq, DEC.D, max_len)
+    wsp = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+    out = torch.empty((B, DEC.Hq, DEC.Sq, DEC.D), dtype=dt, device=dev)
+    lse = torch.empty((B, DEC.Hq, DEC.Sq), dtype=torch.float32, device=dev)
+    q4 = qg.view(B, DEC.Sq, DEC.Hq, DEC.D).permute(0, 2, 1, 3)
+
+    def append():
+        ra.rope_append_kv(cache, qg, kg, vg, pos, cos, sin, layout=DEC.layout)
+
+    def attend():
+        ra.attn_decode(cache, q4, kv_len, max_len, out=out, lse=lse, workspace=wsp)
+
+    for _ in range(args.warmup):
+        append()
+        attend()
+    torch.cuda.synchronize()
+    if ra.ra_get_device_status() != 0:
+        raise RuntimeError("device status error in decode warm-up")
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for s in range(args.steps):
+        ev[s][0].record(stream)
+        append()
+        ev[s][1].record(stream)
+        attend()
+        ev[s][2].record(stream)
+    torch.cuda.synchronize()
+    if ra.ra_get_device_status() != 0:
+        raise RuntimeError("device status error in decode")
+    app_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    att_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    nbytes = DEC.algorithmic_bytes(lens)
+    res = {"B": B, "rows": rows, "append_ms": app_ms, "attn_ms": att_ms,
+           "step_ms": app_ms + att_ms, "bytes": nbytes, "gbs": nbytes / (att_ms * 1e-3) / 1e9,
+           "splits": None if wsb == 0 else "split-KV with merge", "ws_bytes": wsb}
+    if host_e2e:
+        qh, kh, vh = q.pin_memory(), kn.pin_memory(), vn.pin_memory()
+        oh = torch.empty(out.shape, dtype=dt).pin_memory()
+        n = max(1, min(args.steps, 5))
+        for it in range(1 + n):
+            if it == 1:
+                torch.cuda.synchronize()
+                te = time.perf_counter()
+            qg.copy_(qh, non_blocking=True)
+            kg.copy_(kh, non_blocking=True)
+            vg.copy_(vh, non_blocking=True)
+            append()
+            attend()
+            oh.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+        res["e2e_ms"] = (time.perf_counter() - te) / n * 1e3
+        res["h2d"] = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+        res["d2h"] = oh.numel() * oh.element_size()
+    del kc, vc, cache
+    torch.cuda.empty_cache()
+    return res
+
+
+def decode_summary(d, hbm_peak, peak_kind):
+    out = {"workload": DEC.name, "requests": d["B"], "cached_rows": d["rows"],
+           "attn_decode_ms": d["attn_ms"], "rope_append_kv_ms": d["append_ms"],
+           "step_ms": d["step_ms"], "algorithmic_bytes": d["bytes"], "value": d["gbs"],
+           "unit": "GB/s",
+           "roofline": {"bound": "hbm", "achieved": d["gbs"], "peak": hbm_peak, "unit": "GB/s",
+                        "frac": d["gbs"] / hbm_peak,
+                        "traffic": dram_traffic("attn_decode_tc", DECODE_KERNEL_SRC),
+                        "peak_kind": f"{peak_kind} HBM copy",
+                        "note": "attn_decode call (split kernel + merge) over its algorithmic "
+                                "bytes"},
+           "l2": "cache larger than L2"}
+    if "e2e_ms" in d:
+        out["e2e"] = {"ms_per_step": d["e2e_ms"], "h2d_bytes_per_step": d["h2d"],
+                      "d2h_bytes_per_step": d["d2h"]}
+    return out
+
+
 def warm_ms(call, stream, n):
     """Device time per call when calls are pipelined: n calls captured in one
     CUDA graph, one replay timed between two events (no host launch gaps, L2
@@ -431,6 +537,11 @@ def run_ours(args, ws, rank, local):
 
     if args.sweep:
         return run_sweep(ra, args, dev, stream, rank, tf_peak, hbm_peak)
+    if args.only == "decode":
+        d = time_decode(ra, args, dev, stream, host_e2e=False)
+        if rank == 0:
+            print(json.dumps({"only": "decode", **decode_summary(d, hbm_peak, peak_kind)}))
+        return 0
     if args.only == "rope":
         r = time_rope(ra, args, dev, stream)
         if rank == 0:
@@ -447,6 +558,7 @@ def run_ours(args, ws, rank, local):
                               "clocks": a["clocks"]}))
         return 0
     r = time_rope(ra, args, dev, stream)
+    d = time_decode(ra, args, dev, stream)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -476,6 +588,7 @@ def run_ours(args, ws, rank, local):
                                     "traffic": dram_traffic("rope_apply_cb", ROPE_KERNEL_SRC),
                                     "peak_kind": f"{peak_kind} HBM copy"},
                        "l2": "working set 1.4 GB > L2"},
+        "decode_step": decode_summary(d, hbm_peak, peak_kind),
         "cpu_baseline": cpu,
         "e2e": {"value": a["flops"] / a["e2e_s"] / 1e12 * ws, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": a["h2d"], "d2h_bytes_per_step": a["d2h"],
@@ -497,7 +610,9 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=4096)
     ap.add_argument("--ref-rows", type=int, default=2048)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["all", "attn", "rope"], default="all",
+    ap.add_argument("--decode-reqs", type=int, default=0,
+                    help="profiling aid: decode only the first N requests of the decode batch")
+    ap.add_argument("--only", choices=["all", "attn", "rope", "decode"], default="all",
                     help="profiling aid: time one kernel only (no e2e, no CPU baseline)")
     ap.add_argument("--attn-sq", type=int, default=0,
                     help="profiling aid: shrink the attention workload to this many new "

@@ -253,6 +253,14 @@ const char *ra_status_string(ra_status st);
 /* Reason for the last non-OK status returned on this host thread (never NULL). */
 const char *ra_last_error(void);
 
+/*
+ * Kernels launched by the last successful call of attn_fwd_causal_rope,
+ * rope_append_kv or attn_decode on this host thread, space-separated (e.g.
+ * "attn_decode_tc_kernel attn_decode_merge_kernel"); "" before any.  A
+ * dispatch aid (which variant ran); never NULL.  No counterpart on the pages.
+ */
+const char *ra_last_launch(void);
+
 #ifdef __cplusplus
 }
 #endif

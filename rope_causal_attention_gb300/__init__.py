@@ -20,7 +20,7 @@ import torch
 
 __all__ = ["NEOX", "GPTJ", "RAError", "rope_tables_build", "rope_tables_build_scaled",
            "make_tables", "rope_apply_qk", "KVCache", "rope_append_kv", "attn_decode",
-           "attn_decode_workspace_size",
+           "attn_decode_workspace_size", "ra_last_launch",
            "attn_fwd_causal_rope", "ra_get_device_status", "ra_status_string", "library_path",
            "lib"]
 
@@ -94,6 +94,8 @@ def lib():
             L.ra_status_string.restype = ctypes.c_char_p
             L.ra_last_error.argtypes = []
             L.ra_last_error.restype = ctypes.c_char_p
+            L.ra_last_launch.argtypes = []
+            L.ra_last_launch.restype = ctypes.c_char_p
             _lib = L
     return _lib
 
@@ -381,6 +383,11 @@ def attn_decode(cache: KVCache, q, kv_len, max_kv_len: int, seq_ids=None,
         float(softmax_scale) if softmax_scale is not None else 0.0, s3(q), s3(out),
         _ptr(workspace), wbytes, _stream(q.device, stream)), "attn_decode")
     return out, lse
+
+
+def ra_last_launch() -> list[str]:
+    """Kernels the last attention / append / decode call on this thread launched."""
+    return lib().ra_last_launch().decode().split()
 
 
 def ra_get_device_status(stream=None, device=None) -> int:

@@ -19,6 +19,7 @@ namespace {
 __device__ int g_ra_status_word;
 
 thread_local char g_last_error[512] = "no error";
+thread_local char g_last_launch[256] = "";
 
 constexpr int kMaxDevices = 64;
 std::mutex g_status_mu;
@@ -69,6 +70,13 @@ ra_status fail(ra_status st, const char *fmt, ...) {
   vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
   va_end(ap);
   return st;
+}
+
+void clear_launches() { g_last_launch[0] = '\0'; }
+
+void note_launch(const char *kernel) {
+  const size_t n = strlen(g_last_launch);
+  snprintf(g_last_launch + n, sizeof g_last_launch - n, "%s%s", n ? " " : "", kernel);
 }
 
 int *device_status_ptr(cudaError_t *err) {
@@ -169,6 +177,8 @@ const char *ra_status_string(ra_status st) {
 }
 
 const char *ra_last_error(void) { return g_last_error; }
+
+const char *ra_last_launch(void) { return g_last_launch; }
 
 ra_status rope_tables_build(float *cos_out, float *sin_out, int64_t rows, int rot_dim,
                             double base, int freq_dim, cudaStream_t s) {
@@ -357,7 +367,9 @@ ra_status attn_fwd_causal_rope(const void *q, const void *k, const void *v, void
     cudaError_t e;
     a.status = ra::device_status_ptr(&e);
     if (!a.status) return cuda_fail(e, "status word");
+    ra::clear_launches();
     e = ra::launch_attn_simt(a, s);
+    if (e == cudaSuccess) ra::note_launch("attn_simt_kernel");
     return e == cudaSuccess ? RA_OK : cuda_fail(e, "attention (fp32) launch");
   }
   if (D != 64 && D != 128)
@@ -373,7 +385,9 @@ ra_status attn_fwd_causal_rope(const void *q, const void *k, const void *v, void
   cudaError_t e;
   a.status = ra::device_status_ptr(&e);
   if (!a.status) return cuda_fail(e, "status word");
+  ra::clear_launches();
   e = ra::launch_attn_tc(a, s);
+  if (e == cudaSuccess) ra::note_launch("attn_tc_kernel");
   if (e == cudaErrorNotSupported) return fail(RA_ERR_UNSUPPORTED, "no tensor-core variant");
   return e == cudaSuccess ? RA_OK : cuda_fail(e, "attention (tensor core) launch");
 }
@@ -456,6 +470,7 @@ ra_status rope_append_kv(void *q, void *q_out, const void *k_new, const void *v_
   }
   a.seq_ids = seq_ids; a.positions = positions; a.pos_is_int64 = pos_is_int64 ? 1 : 0;
   a.cos_t = cos_t; a.sin_t = sin_t; a.table_rows = table_rows; a.status = status;
+  ra::clear_launches();
   e = ra::launch_rope_append(a, vec, s);
   return e == cudaSuccess ? RA_OK : cuda_fail(e, "rope_append_kv launch");
 }
@@ -543,6 +558,7 @@ ra_status attn_decode(const void *q, void *o, float *lse, const ra_kv_cache *cac
     a.sq[j] = strides_q[j]; a.so[j] = strides_o[j];
   }
   a.workspace = workspace; a.plan = plan;
+  ra::clear_launches();
   e = ra::launch_attn_decode(a, s);
   if (e == cudaErrorNotSupported) return fail(RA_ERR_UNSUPPORTED, "no decode kernel for the case");
   return e == cudaSuccess ? RA_OK : cuda_fail(e, "attn_decode launch");

@@ -33,14 +33,14 @@ constexpr int64_t kSimtChunkMax = 4096;
 
 bool plan_decode(ra_dtype dt, int B, int Hq, int Hkv, int Sq, int D, int64_t max_kv_len,
                  DecodePlan *plan) {
-  if (B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv || Sq < 1 || D < 2 || (D & 1) || D > 256 ||
-      max_kv_len < 1)
+  if (B < 0 || B > 65535 || Hq < 1 || Hkv < 1 || Hkv > 65535 || Hq % Hkv || Sq < 1 || D < 2 ||
+      (D & 1) || D > 256 || max_kv_len < 1)
     return false;
   const int n = (Hq / Hkv) * Sq;  // query rows sharing one kv head
   plan->tc = dt != RA_F32 && D == 128 && n <= 64;
   int64_t chunk_max = kSimtChunkMax;
   if (plan->tc) {
-    const int npad = (n + 15) / 16 * 16;
+    const int npad = n <= 16 ? 16 : (n <= 32 ? 32 : 64);  // the kernel's column widths
     chunk_max = (int64_t)((kDecodeTmemCols - npad) / npad) * 128;
   }
   const int64_t pairs = (int64_t)(B > 0 ? B : 1) * Hkv;
@@ -280,6 +280,7 @@ cudaError_t launch_simt(const DecodeKParams &p, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)p.splits, (unsigned)p.Hkv, (unsigned)p.B);
   attn_decode_simt_kernel<T><<<grid, kWarps * 32, smem, s>>>(p);
+  note_launch("attn_decode_simt_kernel");
   return cudaGetLastError();
 }
 
@@ -289,12 +290,15 @@ cudaError_t launch_merge(const DecodeKParams &p, cudaStream_t s) {
   const int64_t blocks = (rows + 7) / 8;
   if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
   attn_decode_merge_kernel<T><<<(unsigned)blocks, 256, 0, s>>>(p);
+  note_launch("attn_decode_merge_kernel");
   return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t launch_typed(const DecodeArgs &a, cudaStream_t s) {
   const DecodeKParams p = kparams(a);
+  // the tensor-core kernel declines cases it has no variant for (e.g. a cache
+  // too tall for a tensor map); the CUDA-core kernel then runs the same plan
   cudaError_t e = a.plan.tc ? launch_attn_decode_tc(a, s) : cudaErrorNotSupported;
   if (e == cudaErrorNotSupported) e = launch_simt<T>(p, s);
   if (e != cudaSuccess) return e;

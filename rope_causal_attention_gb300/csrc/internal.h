@@ -16,6 +16,11 @@ int *device_status_ptr(cudaError_t *err);
 // Records a readable reason for the current host thread and returns st.
 ra_status fail(ra_status st, const char *fmt, ...);
 
+// Launch record read by ra_last_launch(): cleared at the start of a call,
+// one kernel name appended per launch.
+void clear_launches();
+void note_launch(const char *kernel);
+
 struct TableArgs {
   float *cos_out, *sin_out;
   int64_t rows;

@@ -211,6 +211,7 @@ cudaError_t launch_vec(const AppendKParams &kp, ra_layout layout, cudaStream_t s
     rope_append_vec_kernel<T, RA_NEOX><<<grid, block, 0, s>>>(kp);
   else
     rope_append_vec_kernel<T, RA_GPTJ><<<grid, block, 0, s>>>(kp);
+  note_launch("rope_append_vec_kernel");
   return cudaGetLastError();
 }
 
@@ -220,6 +221,7 @@ cudaError_t launch_scalar(const AppendKParams &kp, ra_layout layout, int tail, c
   const int64_t max_grid = (int64_t)sm_count_current() * 64;
   const unsigned grid = (unsigned)(kp.T < max_grid ? kp.T : max_grid);
   rope_append_scalar_kernel<T><<<grid, block, 0, s>>>(kp, (int)layout, tail);
+  note_launch("rope_append_scalar_kernel");
   return cudaGetLastError();
 }
 

@@ -170,6 +170,9 @@ DECODE_CASES = [
     (torch.bfloat16, 1, 8, 8, 1, 128, [12000]),
     (torch.bfloat16, 2, 4, 4, 1, 64, [100, 1000]),
     (torch.float32, 2, 4, 2, 2, 64, [3, 900]),
+    (torch.bfloat16, 1, 16, 1, 4, 128, [3000]),     # 64 query columns
+    (torch.float16, 2, 20, 2, 4, 128, [700, 41]),   # 40 columns, padded to 64
+    (torch.bfloat16, 2, 24, 2, 2, 128, [1500, 129]),  # 24 columns, padded to 32
     (torch.bfloat16, 1, 64, 1, 2, 128, [300]),      # 128 query rows per kv head
     (torch.float32, 1, 2, 1, 1, 256, [50]),
     (torch.float16, 2, 6, 3, 3, 40, [7, 64]),
@@ -281,3 +284,78 @@ def test_decode_step_end_to_end(ra, orc, dt, layout, rot_dim):
                                    v.float().numpy().transpose(1, 0, 2)[None],
                                    kv_offset=L - Sq, rot_dim=rot_dim, base=base, layout=layout)
         assert np.abs(o[b:b + 1].float().cpu().numpy() - fused_o).max() <= O_TOL[dt]
+
+
+@pytest.mark.parametrize("dt,Hq,Hkv,Sq,D,want", [
+    (torch.bfloat16, 16, 2, 1, 128, "attn_decode_tc_kernel"),
+    (torch.float16, 16, 1, 4, 128, "attn_decode_tc_kernel"),
+    (torch.bfloat16, 8, 2, 1, 64, "attn_decode_simt_kernel"),
+    (torch.float32, 8, 2, 1, 128, "attn_decode_simt_kernel"),
+])
+def test_dispatch_runs_the_expected_kernel(ra, dt, Hq, Hkv, Sq, D, want):
+    """bf16/fp16 with D = 128 run the tcgen05 split kernel (no silent
+    CUDA-core fallback); other cases the CUDA-core kernel; long contexts add
+    the merge."""
+    lens = [3000, 100]
+    cache, starts, ids, q = decode_inputs(ra, dt, 2, Hq, Hkv, Sq, D, lens, "token", seed=31)
+    ra.attn_decode(cache, q.cuda(), torch.tensor(lens, dtype=torch.int32).cuda(), max(lens),
+                   seq_ids=torch.from_numpy(ids).cuda())
+    assert ra.ra_get_device_status() == 0
+    assert ra.ra_last_launch() == [want, "attn_decode_merge_kernel"]
+    _, kn, vn = wl.decode_tokens(1, 1, Hkv, D, dt, seed=3)
+    ra.rope_append_kv(cache, None, kn.cuda(), vn.cuda(), torch.tensor([2], dtype=torch.int32).cuda(),
+                      *ra.make_tables(8, D, 1e4))
+    assert ra.ra_get_device_status() == 0
+    assert ra.ra_last_launch() == ["rope_append_vec_kernel"]
+
+
+def test_decode_workload_full_size_sampled(ra, orc):
+    """The decode workload at full size (512 requests, contexts up to 131072
+    keys, ~140 GB of bf16 K/V) in the launch configuration the benchmark
+    times: append, then decode.  The longest, the shortest and two random
+    requests are checked against the oracle, which rotates the new token's q
+    and k itself (rounded to bf16, the cache's dtype) and reads the other
+    cache rows from the seeded generator's output."""
+    W = wl.DECODE_ATTN
+    if torch.cuda.get_device_properties(0).total_memory < 180e9:
+        pytest.skip("needs the GB300's memory")
+    dev = torch.device("cuda")
+    lens = W.kv_lens()
+    B = lens.shape[0]
+    starts = np.concatenate([[0], np.cumsum(lens)[:-1]]).astype(np.int64)
+    rows = int(lens.sum())
+    g = torch.Generator(device=dev)
+    g.manual_seed(W.seed)
+    kc = torch.randn((rows, W.Hkv, W.D), generator=g, device=dev, dtype=torch.bfloat16)
+    vc = torch.randn((rows, W.Hkv, W.D), generator=g, device=dev, dtype=torch.bfloat16)
+    cache = ra.KVCache(kc, vc, torch.from_numpy(starts).to(dev))
+    q, kn, vn = W.new_tokens()
+    qg = q.cuda()
+    pos = lens - 1
+    cos, sin = ra.make_tables(W.table_rows, W.rot_dim, W.base)
+    ra.rope_append_kv(cache, qg, kn.cuda(), vn.cuda(), torch.from_numpy(pos).to(torch.int32).cuda(),
+                      cos, sin, layout=W.layout)
+    o, lse = ra.attn_decode(cache, qg.view(B, 1, W.Hq, W.D).permute(0, 2, 1, 3),
+                            torch.from_numpy(lens).to(torch.int32).cuda(), int(lens.max()))
+    assert ra.ra_get_device_status() == 0
+    rng = np.random.default_rng(0)
+    picks = [int(np.argmax(lens)), int(np.argmin(lens)), *rng.choice(B, 2, replace=False).tolist()]
+    rnd = lambda x: torch.from_numpy(x).to(torch.bfloat16).float().numpy()
+    for b in picks:
+        L, r0 = int(lens[b]), int(starts[b])
+        k_rows = kc[r0:r0 + L].float().cpu().numpy()
+        v_rows = vc[r0:r0 + L].float().cpu().numpy()
+        # the appended row: the GPU's must be the rotation of k_new; the oracle uses its own
+        check_rotated(kc[r0 + L - 1:r0 + L].cpu(), kn[b:b + 1], pos[b:b + 1], orc, W.rot_dim,
+                      W.base, W.layout)
+        assert torch.equal(vc[r0 + L - 1].cpu(), vn[b])
+        k_rows[L - 1] = rnd(orc.rope_tokens(kn[b:b + 1].float().numpy(), pos[b:b + 1],
+                                            rot_dim=W.rot_dim, base=W.base, layout=W.layout))[0]
+        v_rows[L - 1] = vn[b].float().numpy()
+        q_rot = rnd(orc.rope_tokens(q[b:b + 1].float().numpy(), pos[b:b + 1], rot_dim=W.rot_dim,
+                                    base=W.base, layout=W.layout))
+        want_o, want_lse = orc.decode_attention(q_rot.transpose(1, 0, 2)[None], k_rows, v_rows,
+                                                [0], [L])
+        check_decode(o[b:b + 1], lse[b:b + 1], want_o, want_lse, torch.bfloat16)
+    del kc, vc, cache
+    torch.cuda.empty_cache()

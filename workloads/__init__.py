@@ -162,6 +162,53 @@ class RopeWorkload:
                 + 2 * 4 * (self.rot_dim // 2) * self.T)
 
 
+@dataclass(frozen=True)
+class DecodeWorkload:
+    """One decoder step over a KV cache: B requests, Sq new tokens each; the
+    new token of request b sits at positions()[b] and its context holds
+    kv_lens()[b] = position + Sq keys (the new ones included)."""
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    Sq: int
+    D: int
+    rot_dim: int
+    layout: int
+    base: float
+    table_rows: int
+    dtype: str
+    seed: int
+
+    def positions(self) -> np.ndarray:
+        """Position of each request's first new token (uniform, so that the
+        last new token still has a table row)."""
+        return decode_positions(self.B, self.table_rows - self.Sq, self.seed)
+
+    def kv_lens(self) -> np.ndarray:
+        return self.positions() + self.Sq
+
+    def new_tokens(self):
+        """Token-major q [B*Sq,Hq,D], k and v [B*Sq,Hkv,D] of the new tokens."""
+        return decode_tokens(self.B * self.Sq, self.Hq, self.Hkv, self.D, DTYPES[self.dtype],
+                             self.seed)
+
+    def cache_bytes(self, lens=None) -> int:
+        es = torch.tensor([], dtype=DTYPES[self.dtype]).element_size()
+        lens = self.kv_lens() if lens is None else lens
+        return int(lens.sum()) * self.Hkv * self.D * es * 2
+
+    def algorithmic_bytes(self, lens=None) -> int:
+        """Bytes the decode attention must move: read every cached K and V row
+        of every request once, read q, write O and LSE, read kv_len and
+        seq_start."""
+        es = torch.tensor([], dtype=DTYPES[self.dtype]).element_size()
+        lens = self.kv_lens() if lens is None else lens
+        B = lens.shape[0]
+        return (self.cache_bytes(lens) + 2 * B * self.Hq * self.Sq * self.D * es
+                + 4 * B * self.Hq * self.Sq + 12 * B)
+
+
 # --------------------------------------------------------------- named workloads
 FP32_ATTN = AttnWorkload("fp32_attn_1x2x128x64_neox", 1, 2, 2, 128, 128, 64, "f32", NEOX,
                          10000.0, 0, 1001)
@@ -178,6 +225,12 @@ DECODE_ROPE = RopeWorkload("bf16_rope_decode_T512_64q8kv_D128_r64", 512, 64, 8, 
 
 LONG_GQA = AttnWorkload("bf16_attn_gqa_1x32q8kv_Sq16384_Sk20480_D128_off4096", 1, 32, 8, 16384,
                         20480, 128, "bf16", NEOX, 500000.0, 4096, 1005)
+
+# the decode rope workload's 512 requests (64 q / 8 kv heads, D = 128, r = 64,
+# positions uniform over the 131072-row table) taken one step further: each
+# request attends over its whole context, ~137 GB of bf16 K and V in all
+DECODE_ATTN = DecodeWorkload("bf16_decode_512req_64q8kv_D128_ctx_upto131072", 512, 64, 8, 1, 128,
+                             64, NEOX, 10000.0, 131072, "bf16", 1004)
 
 ALL_ATTN = [FP32_ATTN, *SWEEP, LONG_GQA]
 ALL_ROPE = [CB_ROPE, DECODE_ROPE]
