@@ -240,6 +240,30 @@ ra_status attn_decode(const void *q, void *o, float *lse, const ra_kv_cache *cac
                       size_t workspace_bytes, cudaStream_t s);
 
 /*
+ * attn_decode_noalloc -- attn_decode with its split workspace in a fixed
+ * region of device memory inside the library instead of a caller buffer;
+ * the call itself allocates nothing (no cudaMalloc, no library allocator).
+ * The pages have no counterpart: this is a deployment variant for callers
+ * that must not hand out scratch memory (e.g. inside CUDA-graph capture).
+ *   Same arguments, results and errors as attn_decode without the workspace
+ *   pair.  The region holds RA_DECODE_STATIC_SCRATCH_BYTES; sizes whose
+ *   attn_decode_workspace_size exceeds it return RA_ERR_UNSUPPORTED before
+ *   any CUDA call.  Nothing in the region has to start at zero: each call
+ *   writes every partial result before reading it.
+ *   The region is resolved (cudaGetSymbolAddress) on the first call on each
+ *   device, so that first call must not be made during a stream capture;
+ *   later calls may be captured.  One region per device: calls that may
+ *   overlap in time (different streams, or graphs replayed concurrently)
+ *   race on it and give wrong results; order them on one stream.
+ */
+#define RA_DECODE_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
+ra_status attn_decode_noalloc(const void *q, void *o, float *lse, const ra_kv_cache *cache,
+                              ra_dtype dt, int B, int Hq, int Hkv, int Sq, int D,
+                              const int32_t *seq_ids, const int32_t *kv_len, int64_t max_kv_len,
+                              float softmax_scale, const int64_t strides_q[3],
+                              const int64_t strides_o[3], cudaStream_t s);
+
+/*
  * ra_get_device_status -- synchronise stream s, then read and clear the
  * current device's status word.  Returns RA_OK, the first error a kernel
  * recorded since the last call, or RA_ERR_CUDA if the stream reported an

@@ -20,7 +20,7 @@ import torch
 
 __all__ = ["NEOX", "GPTJ", "RAError", "rope_tables_build", "rope_tables_build_scaled",
            "make_tables", "rope_apply_qk", "KVCache", "rope_append_kv", "attn_decode",
-           "attn_decode_workspace_size", "ra_last_launch",
+           "attn_decode_workspace_size", "attn_decode_noalloc", "ra_last_launch",
            "attn_fwd_causal_rope", "ra_get_device_status", "ra_status_string", "library_path",
            "lib"]
 
@@ -88,6 +88,9 @@ def lib():
             L.attn_decode.argtypes = [vp, vp, vp, cp, i32, i32, i32, i32, i32, i32, vp, vp, i64,
                                       f32, _i64p, _i64p, vp, ctypes.c_size_t, vp]
             L.attn_decode.restype = i32
+            L.attn_decode_noalloc.argtypes = [vp, vp, vp, cp, i32, i32, i32, i32, i32, i32, vp,
+                                              vp, i64, f32, _i64p, _i64p, vp]
+            L.attn_decode_noalloc.restype = i32
             L.ra_get_device_status.argtypes = [vp]
             L.ra_get_device_status.restype = i32
             L.ra_status_string.argtypes = [i32]
@@ -382,6 +385,38 @@ def attn_decode(cache: KVCache, q, kv_len, max_kv_len: int, seq_ids=None,
         _ptr(seq_ids), _ptr(kv_len), int(max_kv_len),
         float(softmax_scale) if softmax_scale is not None else 0.0, s3(q), s3(out),
         _ptr(workspace), wbytes, _stream(q.device, stream)), "attn_decode")
+    return out, lse
+
+
+def attn_decode_noalloc(cache: KVCache, q, kv_len, max_kv_len: int, out, lse=None, seq_ids=None,
+                        softmax_scale: float | None = None, stream=None):
+    """attn_decode with the split workspace in the library's static device
+    region: neither this function nor the library allocates (out, and lse
+    if wanted, are the caller's).  Returns (out, lse)."""
+    for t, n in ((q, "q"), (kv_len, "kv_len"), (seq_ids, "seq_ids"), (out, "out"), (lse, "lse")):
+        _cuda(t, n)
+    if q.dim() != 4 or q.stride(3) != 1:
+        raise ValueError("q must be [B, Hq, Sq, D] with unit last stride")
+    B, Hq, Sq, D = q.shape
+    if q.dtype != cache.k.dtype or D != cache.D:
+        raise ValueError("q must have the cache's dtype and head size")
+    if kv_len.dtype != torch.int32 or kv_len.shape != (B,) or not kv_len.is_contiguous():
+        raise ValueError("kv_len must be contiguous int32 [B]")
+    if seq_ids is not None and (seq_ids.dtype != torch.int32 or seq_ids.shape != (B,)
+                                or not seq_ids.is_contiguous()):
+        raise ValueError("seq_ids must be contiguous int32 [B]")
+    if out is None or out.shape != (B, Hq, Sq, D) or out.dtype != q.dtype or out.stride(3) != 1:
+        raise ValueError("out must be [B, Hq, Sq, D] in q's dtype with unit last stride")
+    if lse is not None and (lse.shape != (B, Hq, Sq) or lse.dtype != torch.float32
+                            or not lse.is_contiguous()):
+        raise ValueError("lse must be contiguous fp32 [B, Hq, Sq]")
+    s3 = lambda t: _arr([t.stride(0), t.stride(1), t.stride(2)])
+    d = cache.desc()
+    _check(lib().attn_decode_noalloc(
+        _ptr(q), _ptr(out), _ptr(lse), ctypes.byref(d), _DT[q.dtype], B, Hq, cache.Hkv, Sq, D,
+        _ptr(seq_ids), _ptr(kv_len), int(max_kv_len),
+        float(softmax_scale) if softmax_scale is not None else 0.0, s3(q), s3(out),
+        _stream(q.device, stream)), "attn_decode_noalloc")
     return out, lse
 
 

@@ -21,6 +21,12 @@ __device__ int g_ra_status_word;
 thread_local char g_last_error[512] = "no error";
 thread_local char g_last_launch[256] = "";
 
+// Split-KV workspace of attn_decode_noalloc: one region per device, resolved
+// once per device with cudaGetSymbolAddress (no allocation at call time).
+static __device__ __align__(256) unsigned char g_decode_scratch[RA_DECODE_STATIC_SCRATCH_BYTES];
+std::mutex g_scratch_mu;
+void *g_scratch_ptr[64];
+
 constexpr int kMaxDevices = 64;
 std::mutex g_status_mu;
 int *g_status_ptr[kMaxDevices];
@@ -77,6 +83,24 @@ void clear_launches() { g_last_launch[0] = '\0'; }
 void note_launch(const char *kernel) {
   const size_t n = strlen(g_last_launch);
   snprintf(g_last_launch + n, sizeof g_last_launch - n, "%s%s", n ? " " : "", kernel);
+}
+
+void *decode_scratch_ptr(cudaError_t *err) {
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= 64) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void *p = nullptr;
+    *err = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (*err != cudaSuccess) return nullptr;
+    g_scratch_ptr[dev] = p;
+  }
+  return g_scratch_ptr[dev];
 }
 
 int *device_status_ptr(cudaError_t *err) {
@@ -562,6 +586,28 @@ ra_status attn_decode(const void *q, void *o, float *lse, const ra_kv_cache *cac
   e = ra::launch_attn_decode(a, s);
   if (e == cudaErrorNotSupported) return fail(RA_ERR_UNSUPPORTED, "no decode kernel for the case");
   return e == cudaSuccess ? RA_OK : cuda_fail(e, "attn_decode launch");
+}
+
+ra_status attn_decode_noalloc(const void *q, void *o, float *lse, const ra_kv_cache *cache,
+                              ra_dtype dt, int B, int Hq, int Hkv, int Sq, int D,
+                              const int32_t *seq_ids, const int32_t *kv_len, int64_t max_kv_len,
+                              float softmax_scale, const int64_t strides_q[3],
+                              const int64_t strides_o[3], cudaStream_t s) {
+  if (!dtype_ok(dt)) return fail(RA_ERR_INVALID_ARG, "unknown dtype %d", (int)dt);
+  ra::DecodePlan plan;
+  if (!ra::plan_decode(dt, B, Hq, Hkv, Sq, D, max_kv_len, &plan))
+    return fail(RA_ERR_INVALID_ARG, "sizes out of range for the split plan");
+  if (plan.ws_bytes > (size_t)RA_DECODE_STATIC_SCRATCH_BYTES)
+    return fail(RA_ERR_UNSUPPORTED, "needs %zu bytes of split workspace, more than the %u-byte "
+                "static region", plan.ws_bytes, (unsigned)RA_DECODE_STATIC_SCRATCH_BYTES);
+  void *ws = nullptr;
+  if (plan.ws_bytes > 0) {
+    cudaError_t e;
+    ws = ra::decode_scratch_ptr(&e);
+    if (!ws) return cuda_fail(e, "static decode workspace");
+  }
+  return attn_decode(q, o, lse, cache, dt, B, Hq, Hkv, Sq, D, seq_ids, kv_len, max_kv_len,
+                     softmax_scale, strides_q, strides_o, ws, plan.ws_bytes, s);
 }
 
 ra_status ra_get_device_status(cudaStream_t s) {

@@ -242,3 +242,16 @@ def test_decode_rejections(L):
     assert decode(L, o=p(8)) == OVERLAP                    # output on top of q
     assert decode(L, o=ctypes.c_void_p(A + (1 << 27))) == OVERLAP      # output on the cache
     assert decode(L, q=p(1)) == ALIGN
+
+
+@no_gpu
+def test_decode_noalloc_rejections(L):
+    """Sizes whose split workspace exceeds the static region are refused
+    before any CUDA call; invalid sizes as in attn_decode."""
+    c = kvc()
+    call = lambda B, Hq, Hkv, maxl: L.attn_decode_noalloc(
+        p(0), p(1 << 22), None, ctypes.byref(c), 1, B, Hq, Hkv, 1, 8, None, p(1 << 24), maxl,
+        ctypes.c_float(0.0), i64(32, 8, 32), i64(32, 8, 32), None)
+    assert call(512, 64, 8, 131072) == UNSUPPORTED
+    assert call(2, 3, 2, 32) == INVALID      # Hq % Hkv
+    assert call(2, 4, 2, 0) == INVALID       # max_kv_len
