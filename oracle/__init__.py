@@ -13,6 +13,8 @@ Contents
   for all rows or a selected subset (C, fp64, threaded over rows).
 * ``decode_attention``: the decoder step's attention over a KV cache of
   already-rotated keys (per sequence, the same naive attention).
+* ``attention_bwd`` (``oracle.backward``): gradients of the fused RoPE
+  attention, probabilities rebuilt from Q and K (numpy, fp64).
 * ``tiled_attention`` (``oracle.tiled``): the Q-block-outer / K-block-inner
   online-softmax recurrence, used only to show that the recurrence reaches
   the naive result.
@@ -217,3 +219,6 @@ def decode_attention(q, k_cache, v_cache, seq_start, kv_len, seq_ids=None,
                            nthreads=nthreads)
         o[b], lse[b] = ob[0], lb[0]
     return o, lse
+
+
+from .backward import attention_bwd  # noqa: E402,F401
