@@ -152,6 +152,49 @@ ra_status attn_fwd_causal_rope(const void *q, const void *k, const void *v, void
                                cudaStream_t s);
 
 /*
+ * attn_bwd_workspace_size -- bytes of device workspace attn_bwd_causal_rope
+ * needs (the fp32 row terms D_i = <dO_i, O_i>, [B][Hq][Sq]); -1 cast to
+ * size_t for invalid sizes.
+ */
+size_t attn_bwd_workspace_size(int B, int Hq, int64_t Sq);
+
+/*
+ * attn_bwd_causal_rope -- gradients of attn_fwd_causal_rope with respect to
+ * the raw (unrotated) q, k and v ([RF] 5: the probabilities are rebuilt from
+ * Q, K and the forward's LSE instead of being stored; [RF] 1-2 for the
+ * rotation).  With q~, k~, s, P, O as in attn_fwd_causal_rope and dO the
+ * gradient of the loss with respect to O:
+ *     dV = P^T dO,  dP = dO V^T,  dS = P o (dP - D),  D_i = <dO_i, O_i>,
+ *     dq~ = scale dS k~,  dk~ = scale dS^T q~,
+ *     dq_i = R(kv_offset + i)^T dq~_i,  dk_j = R(j)^T dk~_j
+ * (R^T: the rotation by the negated angle; dims past rot_dim unrotated); a
+ * kv head's dk, dv sum over the q-heads of its group.  Keys no query sees
+ * get zero gradients.
+ *   q, k, v, layout, rot_dim, tables, kv_offset, softmax_scale: exactly as
+ *   given to the forward call; o: its output; lse: its fp32 LSE [B][Hq][Sq]
+ *   (contiguous); dout: like o.  dq like q, dk like k, dv like v, each with
+ *   its own strides {b, h, s}; written entirely (not accumulated), dtype dt.
+ *   workspace: device, 256-byte aligned, >= attn_bwd_workspace_size bytes,
+ *   contents ignored and clobbered.
+ *   dt RA_F32 runs CUDA-core kernels (D <= 256); RA_BF16 / RA_F16 run the
+ *   tensor-core kernels (D in {64, 128}; 16-byte aligned tensors, strides
+ *   multiples of 8 elements): rotated Q/K and dS enter the products as fp16,
+ *   P, V and dO as dt, accumulation fp32.  Outputs may not overlap any input
+ *   or each other (RA_ERR_OVERLAP).
+ */
+ra_status attn_bwd_causal_rope(const void *q, const void *k, const void *v, const void *o,
+                               const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                               ra_dtype dt, int B, int Hq, int Hkv, int64_t Sq, int64_t Sk, int D,
+                               int64_t kv_offset, int apply_rope, int rot_dim, ra_layout layout,
+                               const float *cos_t, const float *sin_t, int64_t table_rows,
+                               float softmax_scale, const int64_t strides_q[3],
+                               const int64_t strides_k[3], const int64_t strides_v[3],
+                               const int64_t strides_o[3], const int64_t strides_do[3],
+                               const int64_t strides_dq[3], const int64_t strides_dk[3],
+                               const int64_t strides_dv[3], void *workspace,
+                               size_t workspace_bytes, cudaStream_t s);
+
+/*
  * Decoder KV cache ([RF] 2: new K is appended rotated, V unrotated, and cached
  * K is never rotated again).  Row r of head h of the K cache starts at element
  * k[r * k_strides[0] + h * k_strides[1]] (D contiguous elements; likewise V),
@@ -279,7 +322,7 @@ const char *ra_last_error(void);
 
 /*
  * Kernels launched by the last successful call of attn_fwd_causal_rope,
- * rope_append_kv or attn_decode on this host thread, space-separated (e.g.
+ * attn_bwd_causal_rope, rope_append_kv or attn_decode on this host thread, space-separated (e.g.
  * "attn_decode_tc_kernel attn_decode_merge_kernel"); "" before any.  A
  * dispatch aid (which variant ran); never NULL.  No counterpart on the pages.
  */

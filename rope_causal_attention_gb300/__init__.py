@@ -21,7 +21,7 @@ import torch
 __all__ = ["NEOX", "GPTJ", "RAError", "rope_tables_build", "rope_tables_build_scaled",
            "make_tables", "rope_apply_qk", "KVCache", "rope_append_kv", "attn_decode",
            "attn_decode_workspace_size", "attn_decode_noalloc", "ra_last_launch",
-           "attn_fwd_causal_rope", "ra_get_device_status", "ra_status_string", "library_path",
+           "attn_fwd_causal_rope", "attn_bwd_causal_rope", "ra_get_device_status", "ra_status_string", "library_path",
            "lib"]
 
 NEOX = 0
@@ -77,6 +77,12 @@ def lib():
                                                i32, i64, i32, i32, i32, vp, vp, i64, f32,
                                                _i64p, _i64p, _i64p, _i64p, vp]
             L.attn_fwd_causal_rope.restype = i32
+            L.attn_bwd_workspace_size.argtypes = [i32, i32, i64]
+            L.attn_bwd_workspace_size.restype = ctypes.c_size_t
+            L.attn_bwd_causal_rope.argtypes = ([vp] * 9 + [i32, i32, i32, i32, i64, i64, i32, i64,
+                                               i32, i32, i32, vp, vp, i64, f32] + [_i64p] * 8
+                                              + [vp, ctypes.c_size_t, vp])
+            L.attn_bwd_causal_rope.restype = i32
             cp = ctypes.POINTER(KVCacheDesc)
             i32p = ctypes.POINTER(ctypes.c_int32)
             L.rope_append_kv.argtypes = [vp, vp, vp, vp, cp, i32, i64, i32, i32, i32, i32, i32,
@@ -256,6 +262,66 @@ def attn_fwd_causal_rope(q, k, v, cos=None, sin=None, kv_offset: int = 0, apply_
         float(softmax_scale) if softmax_scale is not None else 0.0, s3(q), s3(k), s3(v), s3(out),
         _stream(q.device, stream)), "attn_fwd_causal_rope")
     return out, lse
+
+
+def attn_bwd_causal_rope(q, k, v, o, lse, dout, cos=None, sin=None, kv_offset: int = 0,
+                         apply_rope: bool = True, rot_dim: int | None = None, layout: int = NEOX,
+                         softmax_scale: float | None = None, dq=None, dk=None, dv=None,
+                         workspace=None, stream=None):
+    """Gradients of attn_fwd_causal_rope with respect to the raw q, k, v.
+    o and lse come from the forward call with the same arguments; dout is
+    dL/dO like o.  Returns (dq, dk, dv) in q's dtype."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (lse, "lse"), (dout, "dout"),
+                 (cos, "cos"), (sin, "sin"), (dq, "dq"), (dk, "dk"), (dv, "dv"),
+                 (workspace, "workspace")):
+        _cuda(t, n)
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be 4-D [B, H, S, D]")
+    B, Hq, Sq, D = q.shape
+    _, Hkv, Sk, _ = k.shape
+    if k.shape != (B, Hkv, Sk, D) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, Hkv, Sk, D] with q's B and D")
+    if o.shape != q.shape or dout.shape != q.shape:
+        raise ValueError("o and dout must have q's shape")
+    for t, n in ((k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
+        if t.dtype != q.dtype:
+            raise ValueError(f"{n} must have q's dtype")
+    if q.dtype not in _DT:
+        raise ValueError("dtype must be fp32 / bf16 / fp16")
+    if lse.shape != (B, Hq, Sq) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous fp32 [B, Hq, Sq]")
+    outs = []
+    for t, ref, n in ((dq, q, "dq"), (dk, k, "dk"), (dv, v, "dv")):
+        if t is None:
+            t = torch.empty(ref.shape, dtype=ref.dtype, device=ref.device)
+        elif t.shape != ref.shape or t.dtype != ref.dtype:
+            raise ValueError(f"{n} must match its input's shape and dtype")
+        outs.append(t)
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout"), *zip(outs, ("dq", "dk", "dv"))):
+        if t.stride(3) != 1:
+            raise ValueError(f"{n} needs unit stride in the head dimension")
+    if apply_rope:
+        if cos is None or sin is None:
+            raise ValueError("apply_rope needs the cos/sin tables")
+        rot_dim = 2 * cos.shape[1] if rot_dim is None else int(rot_dim)
+        if rot_dim != 2 * cos.shape[1]:
+            raise ValueError("rot_dim must match the table width")
+        rows = cos.shape[0]
+    else:
+        rot_dim, rows = D, 0
+    need = int(lib().attn_bwd_workspace_size(B, Hq, Sq))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    s3 = lambda t: _arr([t.stride(0), t.stride(1), t.stride(2)])
+    _check(lib().attn_bwd_causal_rope(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(outs[0]), _ptr(outs[1]),
+        _ptr(outs[2]), _DT[q.dtype], B, Hq, Hkv, Sq, Sk, D, int(kv_offset), int(bool(apply_rope)),
+        rot_dim, int(layout), _ptr(cos), _ptr(sin), rows,
+        float(softmax_scale) if softmax_scale is not None else 0.0,
+        s3(q), s3(k), s3(v), s3(o), s3(dout), s3(outs[0]), s3(outs[1]), s3(outs[2]),
+        _ptr(workspace), wbytes, _stream(q.device, stream)), "attn_bwd_causal_rope")
+    return tuple(outs)
 
 
 class KVCache:

@@ -416,6 +416,125 @@ ra_status attn_fwd_causal_rope(const void *q, const void *k, const void *v, void
   return e == cudaSuccess ? RA_OK : cuda_fail(e, "attention (tensor core) launch");
 }
 
+size_t attn_bwd_workspace_size(int B, int Hq, int64_t Sq) {
+  if (B < 0 || Hq < 0 || Sq < 0) return (size_t)-1;
+  return ((size_t)B * Hq * (size_t)Sq * sizeof(float) + 255) / 256 * 256;
+}
+
+ra_status attn_bwd_causal_rope(const void *q, const void *k, const void *v, const void *o,
+                               const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                               ra_dtype dt, int B, int Hq, int Hkv, int64_t Sq, int64_t Sk, int D,
+                               int64_t kv_offset, int apply_rope, int rot_dim, ra_layout layout,
+                               const float *cos_t, const float *sin_t, int64_t table_rows,
+                               float softmax_scale, const int64_t strides_q[3],
+                               const int64_t strides_k[3], const int64_t strides_v[3],
+                               const int64_t strides_o[3], const int64_t strides_do[3],
+                               const int64_t strides_dq[3], const int64_t strides_dk[3],
+                               const int64_t strides_dv[3], void *workspace,
+                               size_t workspace_bytes, cudaStream_t s) {
+  if (!dtype_ok(dt)) return fail(RA_ERR_INVALID_ARG, "unknown dtype %d", (int)dt);
+  if (B < 1 || Hq < 1 || Hkv < 1) return fail(RA_ERR_INVALID_ARG, "B, Hq, Hkv must be >= 1");
+  if (Hq % Hkv) return fail(RA_ERR_INVALID_ARG, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
+  if (Sq < 0 || Sk < 1) return fail(RA_ERR_INVALID_ARG, "need Sq >= 0 and Sk >= 1");
+  if (kv_offset < 0) return fail(RA_ERR_INVALID_ARG, "kv_offset must be >= 0");
+  if (D < 2 || (D & 1)) return fail(RA_ERR_INVALID_ARG, "D must be even and >= 2");
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv)
+    return fail(RA_ERR_INVALID_ARG, "tensors must be non-NULL");
+  const int64_t *st[8] = {strides_q, strides_k, strides_v, strides_o,
+                          strides_do, strides_dq, strides_dk, strides_dv};
+  for (const int64_t *x : st) {
+    if (!x) return fail(RA_ERR_INVALID_ARG, "stride arrays must be non-NULL");
+    for (int j = 0; j < 3; ++j)
+      if (x[j] < 0) return fail(RA_ERR_INVALID_ARG, "strides must be >= 0");
+  }
+  if (apply_rope) {
+    if (!layout_ok(layout)) return fail(RA_ERR_INVALID_ARG, "unknown layout %d", (int)layout);
+    if (rot_dim < 2 || (rot_dim & 1) || rot_dim > D)
+      return fail(RA_ERR_INVALID_ARG, "rot_dim must be even with 2 <= rot_dim <= D");
+    if (!cos_t || !sin_t) return fail(RA_ERR_INVALID_ARG, "tables must be non-NULL");
+    const int64_t need = Sk > kv_offset + Sq ? Sk : kv_offset + Sq;
+    if (table_rows < need)
+      return fail(RA_ERR_INVALID_ARG, "table_rows %lld < needed %lld", (long long)table_rows,
+                  (long long)need);
+    if (!aligned(cos_t, 16) || !aligned(sin_t, 16))
+      return fail(RA_ERR_ALIGNMENT, "tables must be 16-byte aligned");
+  }
+  if (!(softmax_scale <= 0.f) && !isfinite(softmax_scale))
+    return fail(RA_ERR_INVALID_ARG, "softmax_scale must be finite");
+  const size_t need_ws = attn_bwd_workspace_size(B, Hq, Sq);
+  if (Sq > 0 && (!workspace || workspace_bytes < need_ws))
+    return fail(RA_ERR_INVALID_ARG, "workspace of %zu bytes required", need_ws);
+  if (workspace && !aligned(workspace, 256))
+    return fail(RA_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  const size_t es = dtype_size(dt);
+  const void *ptrs[8] = {q, k, v, o, dout, dq, dk, dv};
+  for (const void *x : ptrs)
+    if (!aligned(x, es)) return fail(RA_ERR_ALIGNMENT, "buffers must be element-aligned");
+  if (!aligned(lse, 4)) return fail(RA_ERR_ALIGNMENT, "lse must be 4-byte aligned");
+  // outputs dq, dk, dv and the workspace must not overlap any input or each other
+  {
+    const int64_t lens[8] = {Sq, Sk, Sk, Sq, Sq, Sq, Sk, Sk};
+    const int64_t heads[8] = {Hq, Hkv, Hkv, Hq, Hq, Hq, Hkv, Hkv};
+    int64_t span[8];
+    for (int t = 0; t < 8; ++t)
+      span[t] = lens[t] > 0 ? span4(B, st[t][0], heads[t], st[t][1], lens[t], st[t][2], D, es) : 0;
+    const void *all[10] = {q, k, v, o, dout, lse, dq, dk, dv, workspace};
+    const int64_t n[10] = {span[0], span[1], span[2], span[3], span[4], (int64_t)B * Hq * Sq * 4,
+                           span[5], span[6], span[7], workspace ? (int64_t)need_ws : 0};
+    for (int w = 6; w < 10; ++w) {
+      if (!all[w] || n[w] == 0) continue;
+      for (int r = 0; r < 10; ++r)
+        if (r != w && all[r] && n[r] > 0 && !spans_apart(all[w], n[w], all[r], n[r]))
+          return fail(RA_ERR_OVERLAP, "gradient outputs and workspace must not overlap "
+                                      "anything else");
+    }
+  }
+  if (dt != RA_F32) {
+    if (D != 64 && D != 128)
+      return fail(RA_ERR_UNSUPPORTED, "tensor-core backward supports D in {64, 128} (got %d)", D);
+    if (apply_rope && (layout == RA_NEOX ? (rot_dim / 2) % 8 : rot_dim % 8))
+      return fail(RA_ERR_UNSUPPORTED, "tensor-core backward needs rot_dim/2 %% 8 == 0 (NeoX) "
+                                      "or rot_dim %% 8 == 0 (GPT-J)");
+    for (const void *x : ptrs)
+      if (!aligned(x, 16)) return fail(RA_ERR_ALIGNMENT, "tensor-core backward needs 16-byte "
+                                                         "aligned tensors");
+    for (const int64_t *x : st)
+      for (int j = 0; j < 3; ++j)
+        if (x[j] % 8) return fail(RA_ERR_ALIGNMENT, "tensor-core backward needs strides that "
+                                                    "are multiples of 8");
+  } else if (D > 256) {
+    return fail(RA_ERR_UNSUPPORTED, "fp32 backward supports D <= 256 (got %d)", D);
+  }
+  // keys no query can see still get (zero) gradients, so even Sq == 0 launches
+  ra::BwdArgs a{};
+  ra::AttnArgs &f = a.f;
+  f.q = q; f.k = k; f.v = v; f.dt = dt;
+  f.B = B; f.Hq = Hq; f.Hkv = Hkv; f.Sq = Sq; f.Sk = Sk; f.D = D; f.kv_offset = kv_offset;
+  f.apply_rope = apply_rope ? 1 : 0;
+  f.rot_dim = apply_rope ? rot_dim : D;
+  f.layout = layout_ok(layout) ? layout : RA_NEOX;
+  f.cos_t = cos_t; f.sin_t = sin_t; f.table_rows = table_rows;
+  f.scale = softmax_scale > 0.f ? softmax_scale : (float)(1.0 / sqrt((double)D));
+  for (int j = 0; j < 3; ++j) {
+    f.sq[j] = strides_q[j]; f.sk[j] = strides_k[j]; f.sv[j] = strides_v[j];
+    a.sod[j] = strides_o[j]; a.sdo[j] = strides_do[j]; a.sdq[j] = strides_dq[j];
+    a.sdk[j] = strides_dk[j]; a.sdv[j] = strides_dv[j];
+  }
+  a.o = o; a.dout = dout; a.lse = lse; a.dq = dq; a.dk = dk; a.dv = dv;
+  a.dsum = static_cast<float *>(workspace);
+  cudaError_t e;
+  f.status = ra::device_status_ptr(&e);
+  if (!f.status) return cuda_fail(e, "status word");
+  ra::clear_launches();
+  if (Sq > 0) {
+    e = ra::launch_bwd_rowterm(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "backward row-term launch");
+  }
+  e = dt == RA_F32 ? ra::launch_attn_bwd_simt(a, s) : ra::launch_attn_bwd_tc(a, s);
+  if (e == cudaErrorNotSupported) return fail(RA_ERR_UNSUPPORTED, "no backward kernel for the case");
+  return e == cudaSuccess ? RA_OK : cuda_fail(e, "backward launch");
+}
+
 ra_status rope_append_kv(void *q, void *q_out, const void *k_new, const void *v_new,
                          const ra_kv_cache *cache, ra_dtype dt, int64_t T, int Hq, int Hkv, int D,
                          int rot_dim, ra_layout layout, const int64_t strides_q[2],

@@ -107,7 +107,20 @@ struct DecodeArgs {
   int *status;
 };
 
+struct BwdArgs {
+  AttnArgs f;  // q, k, v, sizes, rope, scale, strides of the forward call
+  const void *o, *dout;
+  const float *lse;
+  void *dq, *dk, *dv;
+  int64_t sod[3], sdo[3], sdq[3], sdk[3], sdv[3];
+  float *dsum;  // workspace: fp32 [B][Hq][Sq]
+};
+
 cudaError_t launch_table_build(const TableArgs &a, cudaStream_t s);
+// D_i = <dO_i, O_i> into a.dsum (any dtype).
+cudaError_t launch_bwd_rowterm(const BwdArgs &a, cudaStream_t s);
+cudaError_t launch_attn_bwd_simt(const BwdArgs &a, cudaStream_t s);
+cudaError_t launch_attn_bwd_tc(const BwdArgs &a, cudaStream_t s);
 cudaError_t launch_rope_append(const AppendArgs &a, bool vectorized, cudaStream_t s);
 // Runs the split kernel (tensor-core or CUDA-core, as planned) and the merge.
 cudaError_t launch_attn_decode(const DecodeArgs &a, cudaStream_t s);

@@ -38,6 +38,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ["rope_tables_build", "rope_tables_build_scaled", "rope_apply_qk", "rope_append_kv",
+              "attn_bwd_causal_rope", "attn_bwd_workspace_size",
               "attn_decode", "attn_decode_workspace_size", "attn_fwd_causal_rope",
               "ra_get_device_status", "ra_status_string", "ra_last_error"]:
         assert n in names

@@ -1,0 +1,129 @@
+"""GPU parity of attn_bwd_causal_rope against the fp64 backward oracle.
+
+Tolerances: gradients compared normwise per tensor, max |got - ref| <=
+tol * max(1, max |ref|) with tol = 1e-4 for fp32 (fp32 accumulation over at
+most a few thousand unit-scale terms) and 2e-2 for bf16 / fp16 (outputs
+rounded to the 16-bit dtype, rotated Q/K and dS rounded to fp16 and P to the
+input dtype before their products, as in the forward's O bound)."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+NEOX, GPTJ = 0, 1
+TOL = {torch.float32: 1e-4, torch.bfloat16: 2e-2, torch.float16: 2e-2}
+
+
+@pytest.fixture(scope="module")
+def ra():
+    import __graft_entry__
+    __graft_entry__.build()
+    import rope_causal_attention_gb300 as m
+    assert m.ra_get_device_status() == 0
+    return m
+
+
+@pytest.fixture(scope="module")
+def orc():
+    import oracle
+    oracle.build()
+    return oracle
+
+
+def grads_case(ra, orc, dt, B, Hq, Hkv, Sq, Sk, D, off, layout, rot_dim, apply_rope=True,
+               scale=None, seed=0, base=10000.0):
+    q, k, v = wl.attn_qkv(B, Hq, Hkv, Sq, Sk, D, dt, seed=seed)
+    g = torch.Generator("cpu").manual_seed(seed + 99)
+    dout = wl.randn((B, Hq, Sq, D), g, dt)
+    qg, kg, vg, dg = q.cuda(), k.cuda(), v.cuda(), dout.cuda()
+    cos = sin = None
+    if apply_rope:
+        cos, sin = ra.make_tables(max(Sk, off + Sq), rot_dim, base)
+    o, lse = ra.attn_fwd_causal_rope(qg, kg, vg, cos, sin, kv_offset=off, apply_rope=apply_rope,
+                                     layout=layout, softmax_scale=scale)
+    dq, dk, dv = ra.attn_bwd_causal_rope(qg, kg, vg, o, lse, dg, cos, sin, kv_offset=off,
+                                         apply_rope=apply_rope, layout=layout,
+                                         softmax_scale=scale)
+    assert ra.ra_get_device_status() == 0
+    want = orc.attention_bwd(q.float().numpy(), k.float().numpy(), v.float().numpy(),
+                             dout.float().numpy(), kv_offset=off, apply_rope=apply_rope,
+                             rot_dim=rot_dim, base=base, layout=layout, scale=scale)
+    for name, got, ref in zip(("dq", "dk", "dv"), (dq, dk, dv), want):
+        err = np.abs(got.float().cpu().numpy().astype(np.float64) - ref).max()
+        bound = TOL[dt] * max(1.0, np.abs(ref).max())
+        assert err <= bound, (name, err, bound)
+    return dq, dk, dv
+
+
+FP32_CASES = [
+    # B, Hq, Hkv, Sq, Sk, D, off, layout, rot_dim
+    (1, 2, 2, 128, 128, 64, 0, NEOX, 64),     # the fp32 workload's shape
+    (2, 4, 2, 50, 70, 64, 20, GPTJ, 32),      # GQA, offset, partial rotation
+    (1, 3, 1, 33, 33, 96, 0, NEOX, 96),
+    (1, 2, 1, 17, 40, 32, 5, GPTJ, 32),       # keys past the last query: zero gradient
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Sk,D,off,layout,rot_dim", FP32_CASES)
+def test_fp32_backward_matches_oracle(ra, orc, B, Hq, Hkv, Sq, Sk, D, off, layout, rot_dim):
+    dq, dk, dv = grads_case(ra, orc, torch.float32, B, Hq, Hkv, Sq, Sk, D, off, layout, rot_dim,
+                            seed=Sq + D)
+    assert ra.ra_last_launch() == ["bwd_rowterm_kernel", "bwd_dq_simt_kernel",
+                                   "bwd_dkdv_simt_kernel"]
+    if Sk > off + Sq:
+        assert bool((dk[:, :, off + Sq:] == 0).all()) and bool((dv[:, :, off + Sq:] == 0).all())
+
+
+def test_fp32_backward_no_rope_custom_scale(ra, orc):
+    grads_case(ra, orc, torch.float32, 1, 4, 2, 40, 60, 64, 20, NEOX, 64, apply_rope=False,
+               scale=0.2, seed=3)
+
+
+def test_fp32_fused_workload(ra, orc):
+    W = wl.FP32_ATTN
+    grads_case(ra, orc, torch.float32, W.B, W.Hq, W.Hkv, W.Sq, W.Sk, W.D, W.kv_offset, W.layout,
+               W.r, seed=W.seed, base=W.base, scale=1.0 / 8)
+
+
+TC_CASES = [
+    # dt, B, Hq, Hkv, Sq, Sk, D, off, layout, rot_dim
+    (torch.bfloat16, 1, 2, 2, 128, 128, 128, 0, NEOX, 128),
+    (torch.bfloat16, 1, 4, 2, 300, 300, 128, 0, GPTJ, 128),
+    (torch.float16, 2, 2, 1, 200, 456, 128, 256, NEOX, 128),
+    (torch.bfloat16, 1, 2, 2, 257, 257, 64, 0, GPTJ, 64),
+    (torch.float16, 1, 4, 4, 130, 200, 64, 70, NEOX, 32),
+    (torch.bfloat16, 1, 8, 2, 512, 512, 128, 0, NEOX, 64),
+    (torch.bfloat16, 1, 2, 1, 100, 400, 128, 100, GPTJ, 128),  # keys past the last query
+]
+
+
+TC_READY = False  # the tensor-core backward kernels are not built yet
+needs_tc = pytest.mark.skipif(not TC_READY, reason="tensor-core backward not built yet")
+
+
+@needs_tc
+@pytest.mark.parametrize("dt,B,Hq,Hkv,Sq,Sk,D,off,layout,rot_dim", TC_CASES)
+def test_tc_backward_matches_oracle(ra, orc, dt, B, Hq, Hkv, Sq, Sk, D, off, layout, rot_dim):
+    grads_case(ra, orc, dt, B, Hq, Hkv, Sq, Sk, D, off, layout, rot_dim, seed=Sq + D + off)
+    assert "bwd_dkdv_tc_kernel" in ra.ra_last_launch()
+    assert "bwd_dq_tc_kernel" in ra.ra_last_launch()
+
+
+@needs_tc
+def test_tc_backward_no_rope(ra, orc):
+    grads_case(ra, orc, torch.bfloat16, 1, 4, 2, 200, 260, 128, 60, NEOX, 128, apply_rope=False,
+               seed=8)
+
+
+def test_backward_rejections(ra):
+    q = torch.zeros((1, 2, 8, 64), dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((1, 2, 8), dtype=torch.float32, device="cuda")
+    with pytest.raises(ra.RAError):  # dq on top of q
+        ra.attn_bwd_causal_rope(q, q, q, q, lse, q, apply_rope=False, dq=q)
+    qd = torch.zeros((1, 2, 8, 96), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ra.RAError) as e:  # tensor-core head sizes
+        ra.attn_bwd_causal_rope(qd, qd, qd, qd, lse, qd, apply_rope=False)
+    assert e.value.code == -2
