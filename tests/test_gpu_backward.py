@@ -100,7 +100,7 @@ TC_CASES = [
 ]
 
 
-TC_READY = False  # the tensor-core backward kernels are not built yet
+TC_READY = True
 needs_tc = pytest.mark.skipif(not TC_READY, reason="tensor-core backward not built yet")
 
 
