@@ -279,6 +279,49 @@ def time_attention(ra, W, args, dev, stream, ws, local, host_e2e=True):
     return out
 
 
+def time_backward(ra, W, args, dev, stream):
+    """Times attn_bwd_causal_rope on workload W (the forward's o and LSE are
+    computed once, untimed); L2 flushed before every timed call.  FLOPs are
+    the algorithmic 2.5x of the forward (the five products S, dP, dV, dK,
+    dQ over the admissible pairs)."""
+    q, k, v = W.inputs()
+    g = torch.Generator("cpu").manual_seed(W.seed + 7)
+    dout = wl.randn((W.B, W.Hq, W.Sq, W.D), g, wl.DTYPES[W.dtype])
+    qg, kg, vg, dg = q.to(dev), k.to(dev), v.to(dev), dout.to(dev)
+    cos, sin = ra.make_tables(max(W.Sk, W.kv_offset + W.Sq), W.r, W.base, device=dev)
+    o, lse = ra.attn_fwd_causal_rope(qg, kg, vg, cos, sin, kv_offset=W.kv_offset, layout=W.layout)
+    dq, dk, dv = torch.empty_like(qg), torch.empty_like(kg), torch.empty_like(vg)
+    wsb = ra.lib().attn_bwd_workspace_size(1, W.B, W.Hq, W.Hkv, W.Sq, W.Sk, W.D)
+    wsp = torch.empty(max(int(wsb), 1), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def call():
+        ra.attn_bwd_causal_rope(qg, kg, vg, o, lse, dg, cos, sin, kv_offset=W.kv_offset,
+                                layout=W.layout, dq=dq, dk=dk, dv=dv, workspace=wsp)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    if ra.ra_get_device_status() != 0:
+        raise RuntimeError("device status error in backward warm-up")
+    ts = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        call()
+        e.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(e))
+    if ra.ra_get_device_status() != 0:
+        raise RuntimeError("device status error in backward")
+    ms = statistics.mean(ts)
+    flops = 2.5 * W.flops()
+    return {"ms": ms, "flops": flops, "tflops": flops / (ms * 1e-3) / 1e12,
+            "kernels": ra.ra_last_launch()}
+
+
 def time_rope(ra, args, dev, stream):
     """Times the in-place rope_apply_qk over the continuous-batching batch
     (its 1.4 GB working set exceeds L2, so no flush is needed)."""
@@ -537,6 +580,14 @@ def run_ours(args, ws, rank, local):
 
     if args.sweep:
         return run_sweep(ra, args, dev, stream, rank, tf_peak, hbm_peak)
+    if args.only == "bwd":
+        W = attn_workload(args)
+        bw = time_backward(ra, W, args, dev, stream)
+        if rank == 0:
+            print(json.dumps({"only": "bwd", "workload": W.name, "ms": bw["ms"],
+                              "TFLOP/s": bw["tflops"], "frac": bw["tflops"] / tf_peak,
+                              "kernels": bw["kernels"]}))
+        return 0
     if args.only == "decode":
         d = time_decode(ra, args, dev, stream, host_e2e=False)
         if rank == 0:
@@ -559,6 +610,7 @@ def run_ours(args, ws, rank, local):
         return 0
     r = time_rope(ra, args, dev, stream)
     d = time_decode(ra, args, dev, stream)
+    bw = time_backward(ra, W, args, dev, stream)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -589,6 +641,16 @@ def run_ours(args, ws, rank, local):
                                     "peak_kind": f"{peak_kind} HBM copy"},
                        "l2": "working set 1.4 GB > L2"},
         "decode_step": decode_summary(d, hbm_peak, peak_kind),
+        "backward": {"workload": W.name, "ms": bw["ms"], "value": bw["tflops"],
+                     "unit": "TFLOP/s", "algorithmic_flops": bw["flops"],
+                     "kernels": bw["kernels"],
+                     "roofline": {"bound": "tensor", "achieved": bw["tflops"], "peak": tf_peak,
+                                  "unit": "TFLOP/s", "frac": bw["tflops"] / tf_peak,
+                                  "traffic": None,
+                                  "peak_kind": f"{peak_kind} bf16 dense (burst)",
+                                  "note": "2.5x the forward's FLOPs (S, dP, dV, dK, dQ); the "
+                                          "kernels recompute S and dP once more for dQ"},
+                     "l2": "flushed before every timed call"},
         "cpu_baseline": cpu,
         "e2e": {"value": a["flops"] / a["e2e_s"] / 1e12 * ws, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": a["h2d"], "d2h_bytes_per_step": a["d2h"],
@@ -612,7 +674,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-reqs", type=int, default=0,
                     help="profiling aid: decode only the first N requests of the decode batch")
-    ap.add_argument("--only", choices=["all", "attn", "rope", "decode"], default="all",
+    ap.add_argument("--only", choices=["all", "attn", "rope", "decode", "bwd"], default="all",
                     help="profiling aid: time one kernel only (no e2e, no CPU baseline)")
     ap.add_argument("--attn-sq", type=int, default=0,
                     help="profiling aid: shrink the attention workload to this many new "

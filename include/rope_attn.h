@@ -153,10 +153,13 @@ ra_status attn_fwd_causal_rope(const void *q, const void *k, const void *v, void
 
 /*
  * attn_bwd_workspace_size -- bytes of device workspace attn_bwd_causal_rope
- * needs (the fp32 row terms D_i = <dO_i, O_i>, [B][Hq][Sq]); -1 cast to
- * size_t for invalid sizes.
+ * needs: the fp32 row terms D_i = <dO_i, O_i> ([B][Hq][Sq]) and, for
+ * bf16/fp16, fp16 copies of the rotated Q ([B][Hq][Sq][D]) and K
+ * ([B][Hkv][Sk][D]) that the tensor-core kernels load tile by tile; -1 cast
+ * to size_t for invalid sizes.
  */
-size_t attn_bwd_workspace_size(int B, int Hq, int64_t Sq);
+size_t attn_bwd_workspace_size(ra_dtype dt, int B, int Hq, int Hkv, int64_t Sq, int64_t Sk,
+                               int D);
 
 /*
  * attn_bwd_causal_rope -- gradients of attn_fwd_causal_rope with respect to

@@ -77,7 +77,7 @@ def lib():
                                                i32, i64, i32, i32, i32, vp, vp, i64, f32,
                                                _i64p, _i64p, _i64p, _i64p, vp]
             L.attn_fwd_causal_rope.restype = i32
-            L.attn_bwd_workspace_size.argtypes = [i32, i32, i64]
+            L.attn_bwd_workspace_size.argtypes = [i32, i32, i32, i32, i64, i64, i32]
             L.attn_bwd_workspace_size.restype = ctypes.c_size_t
             L.attn_bwd_causal_rope.argtypes = ([vp] * 9 + [i32, i32, i32, i32, i64, i64, i32, i64,
                                                i32, i32, i32, vp, vp, i64, f32] + [_i64p] * 8
@@ -309,7 +309,7 @@ def attn_bwd_causal_rope(q, k, v, o, lse, dout, cos=None, sin=None, kv_offset: i
         rows = cos.shape[0]
     else:
         rot_dim, rows = D, 0
-    need = int(lib().attn_bwd_workspace_size(B, Hq, Sq))
+    need = int(lib().attn_bwd_workspace_size(_DT[q.dtype], B, Hq, Hkv, Sq, Sk, D))
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0

@@ -121,6 +121,22 @@ int *device_status_ptr(cudaError_t *err) {
   return g_status_ptr[dev];
 }
 
+bool plan_bwd_workspace(ra_dtype dt, int B, int Hq, int Hkv, int64_t Sq, int64_t Sk, int D,
+                        BwdWorkspace *w) {
+  if (B < 0 || Hq < 0 || Hkv < 0 || Sq < 0 || Sk < 0 || D < 0) return false;
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  size_t off = up((size_t)B * Hq * (size_t)Sq * sizeof(float));  // D_i row terms
+  w->qrot_off = w->krot_off = 0;
+  if (dt != RA_F32) {  // rotated fp16 operands of the tensor-core kernels
+    w->qrot_off = off;
+    off += up((size_t)B * Hq * (size_t)Sq * D * 2);
+    w->krot_off = off;
+    off += up((size_t)B * Hkv * (size_t)Sk * D * 2);
+  }
+  w->bytes = off;
+  return true;
+}
+
 int sm_count_current() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 148;
@@ -416,9 +432,11 @@ ra_status attn_fwd_causal_rope(const void *q, const void *k, const void *v, void
   return e == cudaSuccess ? RA_OK : cuda_fail(e, "attention (tensor core) launch");
 }
 
-size_t attn_bwd_workspace_size(int B, int Hq, int64_t Sq) {
-  if (B < 0 || Hq < 0 || Sq < 0) return (size_t)-1;
-  return ((size_t)B * Hq * (size_t)Sq * sizeof(float) + 255) / 256 * 256;
+size_t attn_bwd_workspace_size(ra_dtype dt, int B, int Hq, int Hkv, int64_t Sq, int64_t Sk,
+                               int D) {
+  ra::BwdWorkspace w;
+  if (!dtype_ok(dt) || !ra::plan_bwd_workspace(dt, B, Hq, Hkv, Sq, Sk, D, &w)) return (size_t)-1;
+  return w.bytes;
 }
 
 ra_status attn_bwd_causal_rope(const void *q, const void *k, const void *v, const void *o,
@@ -461,8 +479,10 @@ ra_status attn_bwd_causal_rope(const void *q, const void *k, const void *v, cons
   }
   if (!(softmax_scale <= 0.f) && !isfinite(softmax_scale))
     return fail(RA_ERR_INVALID_ARG, "softmax_scale must be finite");
-  const size_t need_ws = attn_bwd_workspace_size(B, Hq, Sq);
-  if (Sq > 0 && (!workspace || workspace_bytes < need_ws))
+  ra::BwdWorkspace wsp;
+  ra::plan_bwd_workspace(dt, B, Hq, Hkv, Sq, Sk, D, &wsp);
+  const size_t need_ws = wsp.bytes;
+  if (need_ws > 0 && (!workspace || workspace_bytes < need_ws))
     return fail(RA_ERR_INVALID_ARG, "workspace of %zu bytes required", need_ws);
   if (workspace && !aligned(workspace, 256))
     return fail(RA_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
@@ -522,6 +542,8 @@ ra_status attn_bwd_causal_rope(const void *q, const void *k, const void *v, cons
   }
   a.o = o; a.dout = dout; a.lse = lse; a.dq = dq; a.dk = dk; a.dv = dv;
   a.dsum = static_cast<float *>(workspace);
+  a.qrot = wsp.qrot_off ? static_cast<char *>(workspace) + wsp.qrot_off : nullptr;
+  a.krot = wsp.krot_off ? static_cast<char *>(workspace) + wsp.krot_off : nullptr;
   cudaError_t e;
   f.status = ra::device_status_ptr(&e);
   if (!f.status) return cuda_fail(e, "status word");

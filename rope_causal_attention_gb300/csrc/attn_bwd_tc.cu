@@ -11,7 +11,11 @@
 //   dV = P^T dO,  dk~ = scale dS^T q~,  dq~ = scale dS k~;
 //   dk_j = R(j)^T dk~_j,  dq_i = R(kv_offset + i)^T dq~_i.
 //
-// GB300 design.  Two kernels, neither using atomics:
+// GB300 design.  A memory-bound pass first rotates Q and K once into fp16
+// workspace tensors (every query and key row is used by many tiles, and
+// rotating them tile by tile inside the kernels cost more issue slots than
+// the products), so both kernels load all four operands with TMA.  Then two
+// kernels, neither using atomics:
 //   bwd_dkdv_tc_kernel: one CTA per (key tile of 128 rows, kv head, batch);
 //     K~ and V stay in shared memory, and the CTA walks every (q-head of the
 //     kv group, query tile) that sees its keys.  Per query tile:
@@ -23,18 +27,23 @@
 //     dV and dK~ accumulate in TMEM cols 0..2D-1 over the whole walk, so the
 //     group's q-heads are summed inside the CTA.
 //   bwd_dq_tc_kernel: one CTA per (query tile, q-head, batch); Q~ and dO stay
-//     in shared memory, key tiles stream:
-//       S = Q~ K~^T (cols 0..127),  dP = dO V^T (cols 128..255),
-//       threads: dS (fp16) over S,  dQ~ += dS K~ (TS: B = K~ read MN-major,
-//       TMEM cols 256..256+D-1).
+//     in shared memory, key tiles stream.  S alternates between two TMEM
+//     slots (cols 0..127, 128..255), dP has one (256..383) that the threads
+//     release as soon as they have read it, dQ~ accumulates in 384..: the
+//     MMA order S(n), dP(n), dQ~ += dS(n-1) K~(n-1) lets the tensor core
+//     compute the next tile's S and dP while the threads turn this tile's
+//     into dS.
 //   The epilogues scale, rotate back with R^T (the table's sine negated) and
-//   store in the input dtype.  A shared-memory tile written in the 128-byte
-//   swizzled K-major layout doubles as the MN-major operand of the
-//   transposed product, so Q~, dO and K~ are staged once.
-// Roles (320 threads): warps 0-3 own TMEM lanes 0-127 (probabilities, dS,
-// epilogue), warps 4-7 rotate Q/K rows into fp16 operand tiles, warp 8 issues
-// TMA loads (V, dO), warp 9 allocates TMEM and issues the MMAs.  Every
-// mbarrier wait is bounded (RA_ERR_DEVICE_TIMEOUT, abort flag, drain).
+//   store in the input dtype.  A shared-memory tile in the 128-byte swizzled
+//   K-major layout doubles as the MN-major operand of the transposed product,
+//   so each operand tile is loaded once.
+// Roles (320 threads): warps 0-7 compute P and dS, two warps per TMEM lane
+// quadrant, each on half of the 128 columns (the half-warps pack their
+// 16-bit results into columns they have already read: +0 for the first half,
+// +64 for the second, and the TS products address the two halves per
+// k-step); warp 8 issues the TMA loads (and, for dK/dV, stages the row
+// statistics); warp 9 allocates TMEM and issues the MMAs.  Every mbarrier
+// wait is bounded (RA_ERR_DEVICE_TIMEOUT, abort flag, drain).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -47,66 +56,79 @@
 
 #include "common.cuh"
 #include "internal.h"
-#include "rot_tile.cuh"
 #include "tc_ptx.cuh"
 
 namespace ra {
 namespace {
 
 using namespace ptx;
-using rot::f16x2;
-using rot::In16;
 
 constexpr int kThreads = 320;
-constexpr int kWarpRot = 4, kWarpTma = 8, kWarpMma = 9;
+constexpr int kWarpTma = 8, kWarpMma = 9;
 constexpr uint32_t kTmemCols = 512;
 constexpr long long kTimeoutCycles = 1LL << 32;  // about two seconds
 constexpr float kLog2e = 1.4426950408889634f;
+
+template <typename T> struct Pack16;
+template <> struct Pack16<__nv_bfloat16> {
+  static __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
+  }
+};
+template <> struct Pack16<__half> {
+  static __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
+  }
+};
+__device__ __forceinline__ uint32_t f16x2(float lo, float hi) { return Pack16<__half>::pack2(lo, hi); }
 
 template <int D> struct BCfg {
   static constexpr int TILE = 128 * D * 2;  // 128 rows of 16-bit values
   static constexpr int SUBT = 16384;        // one 64-column sub-tile
   static constexpr int NS = D == 128 ? 2 : 3;
-  // dk/dv kernel: K~ | V | Q~ ring | dO ring | row stats ring (LSE log2, D)
+  // dk/dv kernel: K~ | V | (Q~, dO) ring | row stats ring (LSE log2, D)
   static constexpr int K_OFF_K = 0, K_OFF_V = TILE, K_OFF_Q = 2 * TILE;
   static constexpr int K_OFF_DO = K_OFF_Q + NS * TILE;
   static constexpr int K_OFF_ST = K_OFF_DO + NS * TILE;
   static constexpr int K_OFF_BAR = K_OFF_ST + NS * 1024;
-  // barriers of the dk/dv kernel
-  static constexpr int KB_KFULL = 0, KB_VFULL = 1, KB_QFULL = 2, KB_QEMPTY = 2 + NS,
-                       KB_DOFULL = 2 + 2 * NS, KB_DOEMPTY = 2 + 3 * NS, KB_SFULL = 2 + 4 * NS,
-                       KB_DPFULL = 3 + 4 * NS, KB_PFULL = 4 + 4 * NS, KB_ACC = 5 + 4 * NS,
-                       KB_DONE = 6 + 4 * NS, KB_N = 7 + 4 * NS;
+  static constexpr int KB_KVFULL = 0, KB_QFULL = 1, KB_QEMPTY = 1 + NS, KB_SFULL = 1 + 2 * NS,
+                       KB_DPFULL = 2 + 2 * NS, KB_PFULL = 3 + 2 * NS, KB_ACC = 4 + 2 * NS,
+                       KB_DONE = 5 + 2 * NS, KB_N = 6 + 2 * NS;
   static constexpr int K_OFF_MISC = K_OFF_BAR + KB_N * 8;
   static constexpr int K_SMEM = K_OFF_MISC + 16 + 1024;
-  // dq kernel: Q~ | dO | K~ ring | V ring
+  // dq kernel: Q~ | dO | K~ ring (NSK) | V ring (NSV)
+  static constexpr int NSK = 3, NSV = D == 128 ? 2 : 3;
   static constexpr int Q_OFF_Q = 0, Q_OFF_DO = TILE, Q_OFF_K = 2 * TILE;
-  static constexpr int Q_OFF_V = Q_OFF_K + NS * TILE;
-  static constexpr int Q_OFF_BAR = Q_OFF_V + NS * TILE;
-  static constexpr int QB_QFULL = 0, QB_DOFULL = 1, QB_KFULL = 2, QB_KEMPTY = 2 + NS,
-                       QB_VFULL = 2 + 2 * NS, QB_VEMPTY = 2 + 3 * NS, QB_SFULL = 2 + 4 * NS,
-                       QB_DPFULL = 3 + 4 * NS, QB_PFULL = 4 + 4 * NS, QB_ACC = 5 + 4 * NS,
-                       QB_DONE = 6 + 4 * NS, QB_N = 7 + 4 * NS;
+  static constexpr int Q_OFF_V = Q_OFF_K + NSK * TILE;
+  static constexpr int Q_OFF_BAR = Q_OFF_V + NSV * TILE;
+  static constexpr int QB_QFULL = 0, QB_KFULL = 1, QB_KEMPTY = 1 + NSK,
+                       QB_VFULL = 1 + 2 * NSK, QB_VEMPTY = 1 + 2 * NSK + NSV,
+                       QB_SFULL = 1 + 2 * NSK + 2 * NSV,  // two S slots
+                       QB_DPFULL = 3 + 2 * NSK + 2 * NSV, QB_DPFREE = 4 + 2 * NSK + 2 * NSV,
+                       QB_PFULL = 5 + 2 * NSK + 2 * NSV,  // two S slots
+                       QB_ACC = 7 + 2 * NSK + 2 * NSV, QB_DONE = 8 + 2 * NSK + 2 * NSV,
+                       QB_N = 9 + 2 * NSK + 2 * NSV;
   static constexpr int Q_OFF_MISC = Q_OFF_BAR + QB_N * 8;
   static constexpr int Q_SMEM = Q_OFF_MISC + 16 + 1024;
   static_assert(K_SMEM <= 232448 && Q_SMEM <= 232448, "shared memory");
-  // the epilogue stages 128 padded fp32 rows over the rings
-  static_assert(128 * (D + 1) * 4 <= 2 * NS * TILE, "epilogue scratch");
+  // the epilogues stage 128 padded fp32 rows over the rings
+  static_assert(128 * (D + 1) * 4 <= 2 * NS * TILE && 128 * (D + 1) * 4 <= NSK * TILE,
+                "epilogue scratch");
 };
 
 struct BwdTcParams {
-  const void *q, *k;
   const float *lse, *dsum;
   void *dq, *dk, *dv;
-  int64_t sq0, sq1, sq2, sk0, sk1, sk2;
   int64_t sdq0, sdq1, sdq2, sdk0, sdk1, sdk2, sdv0, sdv1, sdv2;
   int64_t Sq, Sk, off;
   int B, Hq, Hkv, G, n_qt, n_kt;
   int apply_rope, rot_dim, layout;
   const float *cos_t, *sin_t;
-  int64_t table_rows;
   float scale, scale_log2;
-  int vperm[3], operm[3];  // tensor-map dims 1..3 -> logical (0 row, 1 head, 2 batch)
+  // tensor-map dims 1..3 -> logical coordinate (0 row, 1 head, 2 batch)
+  int qperm[3], kperm[3], vperm[3], operm[3];
   int *status;
 };
 
@@ -139,21 +161,14 @@ __device__ __forceinline__ int map_coord(const int perm, int row, int head, int 
   return perm == 0 ? row : (perm == 1 ? head : b);
 }
 
-// One 128-row tile of rows (positions pos0 + r) rotated into a fp16 operand
-// tile by the 128 rotation threads (thread t).
-template <int D, typename TIn>
-__device__ __forceinline__ void rotate_tile(const TIn *rows, int64_t stride, int64_t nvalid,
-                                            int64_t pos0, uint8_t *tile, int t,
-                                            const BwdTcParams &p) {
-  if (p.apply_rope && p.rot_dim == D) {
-    if (p.layout == RA_NEOX)
-      rot::rotate_tile_full<D, TIn, RA_NEOX>(rows, stride, nvalid, pos0, tile, t, p);
-    else
-      rot::rotate_tile_full<D, TIn, RA_GPTJ>(rows, stride, nvalid, pos0, tile, t, p);
-  } else {
-    const bool valid = t < nvalid;
-    rot::rotate_row<D, TIn>(rows + (valid ? t : 0) * stride, valid, pos0 + t, tile, t, p);
-  }
+// One 128-row tile (D/64 boxes of 64 columns) of a [B][H][S][D] tensor map.
+template <int D>
+__device__ __forceinline__ void tma_tile(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                         const int perm[3], int row, int head, int b) {
+#pragma unroll
+  for (int sub = 0; sub < D / 64; ++sub)
+    tma_load_4d(dst + sub * 16384, map, bar, sub * 64, map_coord(perm[0], row, head, b),
+                map_coord(perm[1], row, head, b), map_coord(perm[2], row, head, b));
 }
 
 // Dim e of a padded fp32 row rotated back with R(pos)^T.
@@ -177,29 +192,82 @@ __device__ __forceinline__ float rot_back(const float *row, int e, int64_t pos,
   return low ? row[e] * c + row[partner] * s : row[e] * c - row[partner] * s;
 }
 
-// Stores a D-wide fp32 row (scratch, padded) as dtype, rotated back at pos
-// when `rotate` (16-byte stores).
+// Stores 8-dim groups [g0, g1) of a padded fp32 row as dtype, rotated back
+// at pos when `rotate` (16-byte stores).
 template <int D, typename TIn>
 __device__ __forceinline__ void store_row(const float *row, bool rotate, int64_t pos, TIn *dst,
-                                          const BwdTcParams &p) {
+                                          int g0, int g1, const BwdTcParams &p) {
 #pragma unroll 1
-  for (int g = 0; g < D / 8; ++g) {
+  for (int g = g0; g < g1; ++g) {
     float v[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) v[e] = rotate ? rot_back(row, 8 * g + e, pos, p) : row[8 * g + e];
-    uint4 u;
-    u.x = In16<TIn>::pack2(v[0], v[1]);
-    u.y = In16<TIn>::pack2(v[2], v[3]);
-    u.z = In16<TIn>::pack2(v[4], v[5]);
-    u.w = In16<TIn>::pack2(v[6], v[7]);
-    reinterpret_cast<uint4 *>(dst)[g] = u;
+    reinterpret_cast<uint4 *>(dst)[g] =
+        make_uint4(Pack16<TIn>::pack2(v[0], v[1]), Pack16<TIn>::pack2(v[2], v[3]),
+                   Pack16<TIn>::pack2(v[4], v[5]), Pack16<TIn>::pack2(v[6], v[7]));
+  }
+}
+
+// ================================================================ rotation
+// Rotated fp16 copy of a [B][H][S][D] tensor (row s at position pos0 + s),
+// written contiguous: one thread per 16-byte output chunk (NeoX: a chunk of
+// the low half together with its high-half partner; GPT-J: four pairs);
+// fp32 arithmetic with the fp32 table, one rounding to fp16.
+template <typename TIn>
+__global__ void __launch_bounds__(256) bwd_rotate_f16_kernel(const TIn *__restrict__ x, int H,
+                                                             int64_t S, int D, int64_t s0,
+                                                             int64_t s1, int64_t s2,
+                                                             int64_t pos0, __half *__restrict__ out,
+                                                             int apply_rope, int rot_dim,
+                                                             int layout, const float *cos_t,
+                                                             const float *sin_t, int64_t n) {
+  const int NC = D >> 3;  // chunks per row
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = idx / NC;
+    const int c = (int)(idx - r * NC);
+    const int64_t s = r % S, h = (r / S) % H, b = r / (S * H);
+    const TIn *src = x + b * s0 + h * s1 + s * s2;
+    __half *dst = out + r * D;
+    const int half = rot_dim >> 1;
+    float a[8];
+    unpack16<TIn>(*reinterpret_cast<const uint4 *>(src + 8 * c), a);
+    if (!apply_rope || 8 * c >= rot_dim) {
+      *reinterpret_cast<uint4 *>(dst + 8 * c) = pack16<__half>(a);
+      continue;
+    }
+    const float *cr = cos_t + (pos0 + s) * half, *sr = sin_t + (pos0 + s) * half;
+    if (layout == RA_NEOX) {
+      if (8 * c >= half) continue;  // written by the low-half partner
+      float hb[8], lo[8], hi[8];
+      unpack16<TIn>(*reinterpret_cast<const uint4 *>(src + 8 * c + half), hb);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float cs = __ldg(cr + 8 * c + e), sn = __ldg(sr + 8 * c + e);
+        lo[e] = a[e] * cs - hb[e] * sn;
+        hi[e] = hb[e] * cs + a[e] * sn;
+      }
+      *reinterpret_cast<uint4 *>(dst + 8 * c) = pack16<__half>(lo);
+      *reinterpret_cast<uint4 *>(dst + 8 * c + half) = pack16<__half>(hi);
+    } else {
+      float y[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float cs = __ldg(cr + 4 * c + e), sn = __ldg(sr + 4 * c + e);
+        y[2 * e] = a[2 * e] * cs - a[2 * e + 1] * sn;
+        y[2 * e + 1] = a[2 * e + 1] * cs + a[2 * e] * sn;
+      }
+      *reinterpret_cast<uint4 *>(dst + 8 * c) = pack16<__half>(y);
+    }
   }
 }
 
 // ===================================================================== dK, dV
 template <int D, typename TIn>
 __global__ void __launch_bounds__(kThreads, 1)
-    bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmap_v,
+    bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                       const __grid_constant__ CUtensorMap tmap_k,
+                       const __grid_constant__ CUtensorMap tmap_v,
                        const __grid_constant__ CUtensorMap tmap_do, const BwdTcParams p) {
   using C = BCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -223,17 +291,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int NU = p.G * per_g;  // (q-head, query tile) units
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(C::KB_KFULL), 128);
-    mbar_init(bar(C::KB_VFULL), 1);
+    mbar_init(bar(C::KB_KVFULL), 1);
     for (int i = 0; i < C::NS; ++i) {
-      mbar_init(bar(C::KB_QFULL + i), 128);
+      mbar_init(bar(C::KB_QFULL + i), 33);  // TMA arrive + 32 lanes of row statistics
       mbar_init(bar(C::KB_QEMPTY + i), 1);
-      mbar_init(bar(C::KB_DOFULL + i), 1);
-      mbar_init(bar(C::KB_DOEMPTY + i), 1);
     }
     mbar_init(bar(C::KB_SFULL), 1);
     mbar_init(bar(C::KB_DPFULL), 1);
-    mbar_init(bar(C::KB_PFULL), 128);
+    mbar_init(bar(C::KB_PFULL), 256);
     mbar_init(bar(C::KB_ACC), 1);
     mbar_init(bar(C::KB_DONE), 1);
     *abort_flag = 0;
@@ -244,6 +309,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   if (warp == kWarpTma && lane == 0) {
+    prefetch_tmap(&tmap_q);
+    prefetch_tmap(&tmap_k);
     prefetch_tmap(&tmap_v);
     prefetch_tmap(&tmap_do);
   }
@@ -252,10 +319,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp < 4) {
+  if (warp < 8) {
     // ========================================================= P^T and dS^T
-    const int t = threadIdx.x;
-    const uint32_t lanes = tmem + ((uint32_t)(warp * 32) << 16);
+    const int qd = warp & 3, hf = warp >> 2;
+    const int t = qd * 32 + lane;  // key row of the tile = TMEM lane
+    const uint32_t lanes = tmem + ((uint32_t)(qd * 32) << 16);
     const int64_t j = j0 + t;
     const float sl2 = p.scale_log2;
     bool ok = true;
@@ -267,176 +335,175 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = ok && __all_sync(0xffffffffu, wait_bar(bar(C::KB_DPFULL), (uint32_t)(u & 1), ctl));
       if (!ok) break;
       tc_fence_after();
-      const float *lse2 = reinterpret_cast<const float *>(smem + C::K_OFF_ST + st * 1024);
-      const float *dsm = lse2 + 128;
+      const float4 *lse4 = reinterpret_cast<const float4 *>(smem + C::K_OFF_ST + st * 1024);
+      const float4 *dsm4 = lse4 + 32;
       const int64_t i0 = (int64_t)m * 128;
       const bool straddle = j0 + 127 > p.off + i0;
       const int64_t lim = j - p.off - i0;  // query column c sees key j iff c >= lim
 #pragma unroll 1
-      for (int c0 = 0; c0 < 128; c0 += 32) {
+      for (int bt = 0; bt < 2; ++bt) {
+        const int c0 = 64 * hf + 32 * bt;  // query columns [c0, c0 + 32)
         uint32_t sr[32], dr[32];
         tmem_ld32_pair(lanes + 256u + (uint32_t)c0, lanes + 384u + (uint32_t)c0, sr, dr);
         uint32_t pp[16], pd[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float p0 = ex2(fmaf(__uint_as_float(sr[e]), sl2, -lse2[c0 + e]));
-          float p1 = ex2(fmaf(__uint_as_float(sr[e + 1]), sl2, -lse2[c0 + e + 1]));
-          if (straddle) {
-            if (c0 + e < lim) p0 = 0.f;
-            if (c0 + e + 1 < lim) p1 = 0.f;
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const float4 l4 = lse4[(c0 >> 2) + e4], d4 = dsm4[(c0 >> 2) + e4];
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+          for (int k = 0; k < 4; k += 2) {
+            const int e = 4 * e4 + k;
+            float p0 = ex2(fmaf(__uint_as_float(sr[e]), sl2, -lv[k]));
+            float p1 = ex2(fmaf(__uint_as_float(sr[e + 1]), sl2, -lv[k + 1]));
+            if (straddle) {
+              if (c0 + e < lim) p0 = 0.f;
+              if (c0 + e + 1 < lim) p1 = 0.f;
+            }
+            pp[e >> 1] = Pack16<TIn>::pack2(p0, p1);
+            pd[e >> 1] = f16x2(p0 * (__uint_as_float(dr[e]) - dv[k]),
+                               p1 * (__uint_as_float(dr[e + 1]) - dv[k + 1]));
           }
-          const float d0 = p0 * (__uint_as_float(dr[e]) - dsm[c0 + e]);
-          const float d1 = p1 * (__uint_as_float(dr[e + 1]) - dsm[c0 + e + 1]);
-          pp[e >> 1] = In16<TIn>::pack2(p0, p1);
-          pd[e >> 1] = f16x2(d0, d1);
         }
-        tmem_st16(lanes + 256u + (uint32_t)(c0 >> 1), pp);
-        tmem_st16(lanes + 384u + (uint32_t)(c0 >> 1), pd);
+        // packed into columns this warp has already read: [64 hf + 16 bt, +16)
+        const uint32_t pc = (uint32_t)(64 * hf + 16 * bt);
+        tmem_st16(lanes + 256u + pc, pp);
+        tmem_st16(lanes + 384u + pc, pd);
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(C::KB_PFULL));
     }
-    // ---- epilogue: dV, dK = R(j)^T (scale dK~) for key row j
+    // ---- epilogue: dV straight from TMEM; dK = R(j)^T (scale dK~) through a
+    // padded fp32 row per key (the rotation pairs dims across the halves)
     const bool acc = ok && NU > 0 &&
                      __all_sync(0xffffffffu, wait_bar(bar(C::KB_ACC), 0u, ctl));
-    if (!ok || (NU > 0 && !acc)) goto teardown_k;
+    const bool write = ok && (NU == 0 || acc);
     tc_fence_after();
-    {
-      float *row = reinterpret_cast<float *>(smem + C::K_OFF_Q) + t * (D + 1);
-      TIn *dvd = static_cast<TIn *>(p.dv) + b * p.sdv0 + hk * p.sdv1 + j * p.sdv2;
-      TIn *dkd = static_cast<TIn *>(p.dk) + b * p.sdk0 + hk * p.sdk1 + j * p.sdk2;
-      const bool row_ok = j < p.Sk;
+    float *row = reinterpret_cast<float *>(smem + C::K_OFF_Q) + t * (D + 1);
+    TIn *dvd = static_cast<TIn *>(p.dv) + b * p.sdv0 + hk * p.sdv1 + j * p.sdv2;
+    TIn *dkd = static_cast<TIn *>(p.dk) + b * p.sdk0 + hk * p.sdk1 + j * p.sdk2;
+    const bool row_ok = j < p.Sk;
+    constexpr int HD = D / 2;  // dims per half-warp
 #pragma unroll 1
-      for (int pass = 0; pass < 2; ++pass) {  // 0: dV (cols 0..D-1), 1: dK~ (cols D..2D-1)
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          if (acc) tmem_ld32(lanes + (uint32_t)(pass * D + 32 * c), r);
+    for (int c = 0; c < HD / 32; ++c) {
+      const int col = HD * hf + 32 * c;
+      uint32_t r[32];
+      if (acc) tmem_ld32(lanes + (uint32_t)col, r);
+      if (write && row_ok) {
+        uint4 *d4 = reinterpret_cast<uint4 *>(dvd + col);
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            row[32 * c + e] = acc ? __uint_as_float(r[e]) * (pass ? p.scale : 1.f) : 0.f;
+        for (int g = 0; g < 4; ++g) {
+          float v[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[e] = acc ? __uint_as_float(r[8 * g + e]) : 0.f;
+          d4[g] = make_uint4(Pack16<TIn>::pack2(v[0], v[1]), Pack16<TIn>::pack2(v[2], v[3]),
+                             Pack16<TIn>::pack2(v[4], v[5]), Pack16<TIn>::pack2(v[6], v[7]));
         }
-        if (row_ok) store_row<D, TIn>(row, pass == 1, j, pass ? dkd : dvd, p);
       }
+      if (acc) tmem_ld32(lanes + (uint32_t)(D + col), r);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) row[col + e] = acc ? __uint_as_float(r[e]) * p.scale : 0.f;
     }
-  teardown_k:;
-  } else if (warp < 8) {
-    // ============================================================== rotation
-    const int t = threadIdx.x - kWarpRot * 32;
-    const TIn *kb = static_cast<const TIn *>(p.k) + b * p.sk0 + hk * p.sk1 + j0 * p.sk2;
-    rotate_tile<D, TIn>(kb, p.sk2, p.Sk - j0, j0, smem + C::K_OFF_K, t, p);
-    fence_proxy_async_smem();
-    mbar_arrive(bar(C::KB_KFULL));
+    named_bar_sync(1, 256);  // both halves of every row are in shared memory
+    if (write && row_ok) store_row<D, TIn>(row, true, j, dkd, hf * (D / 16), (hf + 1) * (D / 16), p);
+  } else if (warp == kWarpTma) {
+    // ============================================= TMA and row statistics
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar(C::KB_KVFULL), (uint32_t)(2 * C::TILE));
+      tma_tile<D>(sbase + C::K_OFF_K, &tmap_k, bar(C::KB_KVFULL), p.kperm, (int)j0, hk, b);
+      tma_tile<D>(sbase + C::K_OFF_V, &tmap_v, bar(C::KB_KVFULL), p.vperm, (int)j0, hk, b);
+    }
+    int issued = 0;
     for (int u = 0; u < NU; ++u) {
       const int st = u % C::NS;
       if (u >= C::NS &&
-          !wait_bar(bar(C::KB_QEMPTY + st), (uint32_t)((u / C::NS - 1) & 1), ctl))
+          !__all_sync(0xffffffffu, wait_bar(bar(C::KB_QEMPTY + st), (uint32_t)((u / C::NS - 1) & 1), ctl)))
         break;
       const int g = u / per_g, m = m_first + u % per_g, h = hk * p.G + g;
-      const int64_t i0 = (int64_t)m * 128;
-      const TIn *qb = static_cast<const TIn *>(p.q) + b * p.sq0 + h * p.sq1 + i0 * p.sq2;
-      rotate_tile<D, TIn>(qb, p.sq2, p.Sq - i0, p.off + i0, smem + C::K_OFF_Q + st * C::TILE, t, p);
-      float *stats = reinterpret_cast<float *>(smem + C::K_OFF_ST + st * 1024);
-      const int64_t i = i0 + t;
-      const int64_t r = ((int64_t)b * p.Hq + h) * p.Sq + i;
-      stats[t] = i < p.Sq ? p.lse[r] * kLog2e : INFINITY;  // rows past Sq: P = 0
-      stats[128 + t] = i < p.Sq ? p.dsum[r] : 0.f;
-      fence_proxy_async_smem();
-      mbar_arrive(bar(C::KB_QFULL + st));
-    }
-  } else if (warp == kWarpTma) {
-    // =================================================================== TMA
-    if (lane == 0) {
-      mbar_arrive_expect_tx(bar(C::KB_VFULL), (uint32_t)C::TILE);
-#pragma unroll
-      for (int sub = 0; sub < D / 64; ++sub)
-        tma_load_4d(sbase + C::K_OFF_V + sub * C::SUBT, &tmap_v, bar(C::KB_VFULL), sub * 64,
-                    map_coord(p.vperm[0], (int)j0, hk, b), map_coord(p.vperm[1], (int)j0, hk, b),
-                    map_coord(p.vperm[2], (int)j0, hk, b));
-      int issued = 0;
-      for (int u = 0; u < NU; ++u) {
-        const int st = u % C::NS;
-        if (u >= C::NS &&
-            !wait_bar(bar(C::KB_DOEMPTY + st), (uint32_t)((u / C::NS - 1) & 1), ctl))
-          break;
-        const int g = u / per_g, m = m_first + u % per_g, h = hk * p.G + g;
-        const int row = m * 128;
-        mbar_arrive_expect_tx(bar(C::KB_DOFULL + st), (uint32_t)C::TILE);
-#pragma unroll
-        for (int sub = 0; sub < D / 64; ++sub)
-          tma_load_4d(sbase + C::K_OFF_DO + st * C::TILE + sub * C::SUBT, &tmap_do,
-                      bar(C::KB_DOFULL + st), sub * 64, map_coord(p.operm[0], row, h, b),
-                      map_coord(p.operm[1], row, h, b), map_coord(p.operm[2], row, h, b));
-        issued = u + 1;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(C::KB_QFULL + st), (uint32_t)(2 * C::TILE));
+        tma_tile<D>(sbase + C::K_OFF_Q + st * C::TILE, &tmap_q, bar(C::KB_QFULL + st), p.qperm,
+                    m * 128, h, b);
+        tma_tile<D>(sbase + C::K_OFF_DO + st * C::TILE, &tmap_do, bar(C::KB_QFULL + st), p.operm,
+                    m * 128, h, b);
       }
-      // copies in flight land before the block exits
-      wait_bar_drain(bar(C::KB_VFULL), 0u);
+      // LSE (log2 units) and D of the tile's 128 rows; rows past Sq get P = 0
+      float *sv = reinterpret_cast<float *>(smem + C::K_OFF_ST + st * 1024);
+      const int64_t rb = ((int64_t)b * p.Hq + h) * p.Sq + (int64_t)m * 128;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int t = lane + 32 * k;
+        const bool in = (int64_t)m * 128 + t < p.Sq;
+        sv[t] = in ? p.lse[rb + t] * kLog2e : INFINITY;
+        sv[128 + t] = in ? p.dsum[rb + t] : 0.f;
+      }
+      mbar_arrive(bar(C::KB_QFULL + st));
+      issued = u + 1;
+    }
+    if (lane == 0) {  // copies in flight land before the block exits
+      wait_bar_drain(bar(C::KB_KVFULL), 0u);
       if (*abort_flag)
         for (int u = max(0, issued - C::NS); u < issued; ++u)
-          wait_bar_drain(bar(C::KB_DOFULL + u % C::NS), (uint32_t)((u / C::NS) & 1));
+          wait_bar_drain(bar(C::KB_QFULL + u % C::NS), (uint32_t)((u / C::NS) & 1));
     }
-  } else {
+  } else if (lane == 0) {
     // =================================================================== MMA
-    if (lane == 0) {
-      constexpr uint32_t ab = std::is_same<TIn, __nv_bfloat16>::value ? 1u : 0u;
-      constexpr uint32_t IDESC_S = idesc_f16(0u, 0u, 128);   // fp16 K~ x Q~^T
-      constexpr uint32_t IDESC_DP = idesc_f16(ab, 0u, 128);  // V x dO^T
-      constexpr uint32_t IDESC_DV = idesc_f16(ab, 1u, D);    // P^T x dO (dO MN-major)
-      constexpr uint32_t IDESC_DK = idesc_f16(0u, 1u, D);    // dS^T x Q~ (Q~ MN-major)
-      constexpr uint32_t HI = sdesc_hi_sw128(1024);
-      const uint32_t k_lo = sdesc_lo(sbase + C::K_OFF_K, 16);
-      const uint32_t v_lo = sdesc_lo(sbase + C::K_OFF_V, 16);
-      const uint32_t q_lo0 = sdesc_lo(sbase + C::K_OFF_Q, 16);
-      const uint32_t do_lo0 = sdesc_lo(sbase + C::K_OFF_DO, 16);
-      const uint32_t qmn_lo0 = sdesc_lo(sbase + C::K_OFF_Q, C::SUBT);
-      const uint32_t domn_lo0 = sdesc_lo(sbase + C::K_OFF_DO, C::SUBT);
-      bool ok = NU == 0 || (wait_bar(bar(C::KB_KFULL), 0u, ctl) && wait_bar(bar(C::KB_VFULL), 0u, ctl));
-      for (int u = 0; ok && u < NU; ++u) {
-        const int st = u % C::NS;
-        if (!wait_bar(bar(C::KB_QFULL + st), (uint32_t)((u / C::NS) & 1), ctl) ||
-            !wait_bar(bar(C::KB_DOFULL + st), (uint32_t)((u / C::NS) & 1), ctl)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t so = (uint32_t)(st * C::TILE >> 4);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (uint32_t)(((kk >> 2) * C::SUBT + (kk & 3) * 32) >> 4);
-          mma_ss(tmem + 256u, sdesc_join(k_lo + off, HI), sdesc_join(q_lo0 + so + off, HI),
-                 IDESC_S, kk > 0 ? 1u : 0u);
-        }
-        tc_commit(bar(C::KB_SFULL));
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (uint32_t)(((kk >> 2) * C::SUBT + (kk & 3) * 32) >> 4);
-          mma_ss(tmem + 384u, sdesc_join(v_lo + off, HI), sdesc_join(do_lo0 + so + off, HI),
-                 IDESC_DP, kk > 0 ? 1u : 0u);
-        }
-        tc_commit(bar(C::KB_DPFULL));
-        if (!wait_bar(bar(C::KB_PFULL), (uint32_t)(u & 1), ctl)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // 16 queries per step
-          mma_ts(tmem, tmem + 256u + (uint32_t)(kk * 8),
-                 sdesc_join(domn_lo0 + so + (uint32_t)(kk * 2048 >> 4), HI), IDESC_DV,
-                 (u > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + (uint32_t)D, tmem + 384u + (uint32_t)(kk * 8),
-                 sdesc_join(qmn_lo0 + so + (uint32_t)(kk * 2048 >> 4), HI), IDESC_DK,
-                 (u > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(bar(C::KB_QEMPTY + st));
-        tc_commit(bar(C::KB_DOEMPTY + st));
+    constexpr uint32_t ab = std::is_same<TIn, __nv_bfloat16>::value ? 1u : 0u;
+    constexpr uint32_t IDESC_S = idesc_f16(0u, 0u, 128);   // fp16 K~ x Q~^T
+    constexpr uint32_t IDESC_DP = idesc_f16(ab, 0u, 128);  // V x dO^T
+    constexpr uint32_t IDESC_DV = idesc_f16(ab, 1u, D);    // P^T x dO (dO MN-major)
+    constexpr uint32_t IDESC_DK = idesc_f16(0u, 1u, D);    // dS^T x Q~ (Q~ MN-major)
+    constexpr uint32_t HI = sdesc_hi_sw128(1024);
+    const uint32_t k_lo = sdesc_lo(sbase + C::K_OFF_K, 16);
+    const uint32_t v_lo = sdesc_lo(sbase + C::K_OFF_V, 16);
+    const uint32_t q_lo0 = sdesc_lo(sbase + C::K_OFF_Q, 16);
+    const uint32_t do_lo0 = sdesc_lo(sbase + C::K_OFF_DO, 16);
+    const uint32_t qmn_lo0 = sdesc_lo(sbase + C::K_OFF_Q, C::SUBT);
+    const uint32_t domn_lo0 = sdesc_lo(sbase + C::K_OFF_DO, C::SUBT);
+    bool ok = NU == 0 || wait_bar(bar(C::KB_KVFULL), 0u, ctl);
+    for (int u = 0; ok && u < NU; ++u) {
+      const int st = u % C::NS;
+      if (!wait_bar(bar(C::KB_QFULL + st), (uint32_t)((u / C::NS) & 1), ctl)) {
+        ok = false;
+        break;
       }
-      if (ok && NU > 0) tc_commit(bar(C::KB_ACC));
-      tc_commit(bar(C::KB_DONE));
-      wait_bar_drain(bar(C::KB_DONE), 0u);
+      tc_fence_after();
+      const uint32_t so = (uint32_t)(st * C::TILE >> 4);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (uint32_t)(((kk >> 2) * C::SUBT + (kk & 3) * 32) >> 4);
+        mma_ss(tmem + 256u, sdesc_join(k_lo + off, HI), sdesc_join(q_lo0 + so + off, HI),
+               IDESC_S, kk > 0 ? 1u : 0u);
+      }
+      tc_commit(bar(C::KB_SFULL));
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (uint32_t)(((kk >> 2) * C::SUBT + (kk & 3) * 32) >> 4);
+        mma_ss(tmem + 384u, sdesc_join(v_lo + off, HI), sdesc_join(do_lo0 + so + off, HI),
+               IDESC_DP, kk > 0 ? 1u : 0u);
+      }
+      tc_commit(bar(C::KB_DPFULL));
+      if (!wait_bar(bar(C::KB_PFULL), (uint32_t)(u & 1), ctl)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // 16 queries per step; queries 64..127 were packed at column +64
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ts(tmem, tmem + 256u + (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8),
+               sdesc_join(domn_lo0 + so + (uint32_t)(kk * 2048 >> 4), HI), IDESC_DV,
+               (u > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ts(tmem + (uint32_t)D, tmem + 384u + (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8),
+               sdesc_join(qmn_lo0 + so + (uint32_t)(kk * 2048 >> 4), HI), IDESC_DK,
+               (u > 0 || kk > 0) ? 1u : 0u);
+      tc_commit(bar(C::KB_QEMPTY + st));
     }
+    if (ok && NU > 0) tc_commit(bar(C::KB_ACC));
+    tc_commit(bar(C::KB_DONE));
+    wait_bar_drain(bar(C::KB_DONE), 0u);
   }
 
   tc_fence_before();
@@ -448,7 +515,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ========================================================================= dQ
 template <int D, typename TIn>
 __global__ void __launch_bounds__(kThreads, 1)
-    bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmap_v,
+    bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                     const __grid_constant__ CUtensorMap tmap_k,
+                     const __grid_constant__ CUtensorMap tmap_v,
                      const __grid_constant__ CUtensorMap tmap_do, const BwdTcParams p) {
   using C = BCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -471,17 +540,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int N = (int)min((int64_t)p.n_kt, last_pos / 128 + 1);  // key tiles seen (>= 1)
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(C::QB_QFULL), 128);
-    mbar_init(bar(C::QB_DOFULL), 1);
-    for (int i = 0; i < C::NS; ++i) {
-      mbar_init(bar(C::QB_KFULL + i), 128);
+    mbar_init(bar(C::QB_QFULL), 1);
+    for (int i = 0; i < C::NSK; ++i) {
+      mbar_init(bar(C::QB_KFULL + i), 1);
       mbar_init(bar(C::QB_KEMPTY + i), 1);
+    }
+    for (int i = 0; i < C::NSV; ++i) {
       mbar_init(bar(C::QB_VFULL + i), 1);
       mbar_init(bar(C::QB_VEMPTY + i), 1);
     }
-    mbar_init(bar(C::QB_SFULL), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(C::QB_SFULL + i), 1);
+      mbar_init(bar(C::QB_PFULL + i), 256);
+    }
     mbar_init(bar(C::QB_DPFULL), 1);
-    mbar_init(bar(C::QB_PFULL), 128);
+    mbar_init(bar(C::QB_DPFREE), 256);
     mbar_init(bar(C::QB_ACC), 1);
     mbar_init(bar(C::QB_DONE), 1);
     *abort_flag = 0;
@@ -492,6 +565,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   if (warp == kWarpTma && lane == 0) {
+    prefetch_tmap(&tmap_q);
+    prefetch_tmap(&tmap_k);
     prefetch_tmap(&tmap_v);
     prefetch_tmap(&tmap_do);
   }
@@ -500,10 +575,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp < 4) {
+  if (warp < 8) {
     // ================================================================== dS
-    const int t = threadIdx.x;
-    const uint32_t lanes = tmem + ((uint32_t)(warp * 32) << 16);
+    const int qd = warp & 3, hf = warp >> 2;
+    const int t = qd * 32 + lane;  // query row of the tile = TMEM lane
+    const uint32_t lanes = tmem + ((uint32_t)(qd * 32) << 16);
     const int64_t i = i0 + t;
     const bool row_ok = i < p.Sq;
     const int64_t r = ((int64_t)b * p.Hq + h) * p.Sq + i;
@@ -513,18 +589,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t qpos = p.off + i;
     bool ok = true;
     for (int n = 0; n < N; ++n) {
-      ok = ok && __all_sync(0xffffffffu, wait_bar(bar(C::QB_SFULL), (uint32_t)(n & 1), ctl));
+      const int sl = n & 1;  // S slot of this key tile (TMEM cols 128 sl ..)
+      ok = ok && __all_sync(0xffffffffu, wait_bar(bar(C::QB_SFULL + sl), (uint32_t)((n >> 1) & 1), ctl));
       ok = ok && __all_sync(0xffffffffu, wait_bar(bar(C::QB_DPFULL), (uint32_t)(n & 1), ctl));
       if (!ok) break;
       tc_fence_after();
+      // dP first, then release its columns so the next tile's dP can start
+      uint32_t dr[64];
+      tmem_ld64(lanes + 256u + (uint32_t)(64 * hf), dr);
+      tc_fence_before();
+      mbar_arrive(bar(C::QB_DPFREE));
       const int64_t jt = (int64_t)n * 128;
       const bool straddle = (jt + 127 > p.off + i0) || (jt + 127 >= p.Sk);
       // key column c is admissible iff c <= lim
       const int64_t lim = min(qpos, p.Sk - 1) - jt;
-#pragma unroll 1
-      for (int c0 = 0; c0 < 128; c0 += 32) {
-        uint32_t sr[32], dr[32];
-        tmem_ld32_pair(lanes + (uint32_t)c0, lanes + 128u + (uint32_t)c0, sr, dr);
+      const uint32_t sbase_t = lanes + (uint32_t)(128 * sl);
+#pragma unroll
+      for (int bt = 0; bt < 2; ++bt) {
+        const int c0 = 64 * hf + 32 * bt;  // key columns [c0, c0 + 32)
+        uint32_t sr[32];
+        tmem_ld32(sbase_t + (uint32_t)c0, sr);
         uint32_t pd[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
@@ -534,133 +618,153 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (c0 + e > lim) p0 = 0.f;
             if (c0 + e + 1 > lim) p1 = 0.f;
           }
-          pd[e >> 1] = f16x2(p0 * (__uint_as_float(dr[e]) - dsum),
-                             p1 * (__uint_as_float(dr[e + 1]) - dsum));
+          pd[e >> 1] = f16x2(p0 * (__uint_as_float(dr[32 * bt + e]) - dsum),
+                             p1 * (__uint_as_float(dr[32 * bt + e + 1]) - dsum));
         }
-        tmem_st16(lanes + (uint32_t)(c0 >> 1), pd);
+        // packed into columns this warp has already read: [64 hf + 16 bt, +16)
+        tmem_st16(sbase_t + (uint32_t)(64 * hf + 16 * bt), pd);
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(C::QB_PFULL));
+      mbar_arrive(bar(C::QB_PFULL + sl));
     }
-    // ---- epilogue: dq = R(kv_offset + i)^T (scale dQ~)
+    // ---- epilogue: dq = R(kv_offset + i)^T (scale dQ~) through a padded row
     const bool acc = ok && __all_sync(0xffffffffu, wait_bar(bar(C::QB_ACC), 0u, ctl));
-    if (acc) {
-      tc_fence_after();
-      float *row = reinterpret_cast<float *>(smem + C::Q_OFF_K) + t * (D + 1);
+    tc_fence_after();
+    float *row = reinterpret_cast<float *>(smem + C::Q_OFF_K) + t * (D + 1);
+    constexpr int HD = D / 2;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t rr[32];
-        tmem_ld32(lanes + 256u + (uint32_t)(32 * c), rr);
+    for (int c = 0; c < HD / 32; ++c) {
+      const int col = HD * hf + 32 * c;
+      uint32_t rr[32];
+      if (acc) tmem_ld32(lanes + 384u + (uint32_t)col, rr);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) row[32 * c + e] = __uint_as_float(rr[e]) * p.scale;
-      }
-      if (row_ok)
-        store_row<D, TIn>(row, true, qpos,
-                          static_cast<TIn *>(p.dq) + b * p.sdq0 + h * p.sdq1 + i * p.sdq2, p);
+      for (int e = 0; e < 32; ++e) row[col + e] = acc ? __uint_as_float(rr[e]) * p.scale : 0.f;
     }
-  } else if (warp < 8) {
-    // ============================================================== rotation
-    const int t = threadIdx.x - kWarpRot * 32;
-    const TIn *qb = static_cast<const TIn *>(p.q) + b * p.sq0 + h * p.sq1 + i0 * p.sq2;
-    rotate_tile<D, TIn>(qb, p.sq2, p.Sq - i0, p.off + i0, smem + C::Q_OFF_Q, t, p);
-    fence_proxy_async_smem();
-    mbar_arrive(bar(C::QB_QFULL));
-    const TIn *kb = static_cast<const TIn *>(p.k) + b * p.sk0 + hk * p.sk1;
-    for (int n = 0; n < N; ++n) {
-      const int st = n % C::NS;
-      if (n >= C::NS &&
-          !wait_bar(bar(C::QB_KEMPTY + st), (uint32_t)((n / C::NS - 1) & 1), ctl))
-        break;
-      const int64_t jt = (int64_t)n * 128;
-      rotate_tile<D, TIn>(kb + jt * p.sk2, p.sk2, p.Sk - jt, jt, smem + C::Q_OFF_K + st * C::TILE,
-                          t, p);
-      fence_proxy_async_smem();
-      mbar_arrive(bar(C::QB_KFULL + st));
-    }
+    named_bar_sync(1, 256);  // both halves of every row are in shared memory
+    if (acc && row_ok)
+      store_row<D, TIn>(row, true, qpos,
+                        static_cast<TIn *>(p.dq) + b * p.sdq0 + h * p.sdq1 + i * p.sdq2,
+                        hf * (D / 16), (hf + 1) * (D / 16), p);
   } else if (warp == kWarpTma) {
     // =================================================================== TMA
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar(C::QB_DOFULL), (uint32_t)C::TILE);
-#pragma unroll
-      for (int sub = 0; sub < D / 64; ++sub)
-        tma_load_4d(sbase + C::Q_OFF_DO + sub * C::SUBT, &tmap_do, bar(C::QB_DOFULL), sub * 64,
-                    map_coord(p.operm[0], (int)i0, h, b), map_coord(p.operm[1], (int)i0, h, b),
-                    map_coord(p.operm[2], (int)i0, h, b));
-      int issued = 0;
-      for (int n = 0; n < N; ++n) {
-        const int st = n % C::NS;
-        if (n >= C::NS &&
-            !wait_bar(bar(C::QB_VEMPTY + st), (uint32_t)((n / C::NS - 1) & 1), ctl))
-          break;
-        const int row = n * 128;
-        mbar_arrive_expect_tx(bar(C::QB_VFULL + st), (uint32_t)C::TILE);
-#pragma unroll
-        for (int sub = 0; sub < D / 64; ++sub)
-          tma_load_4d(sbase + C::Q_OFF_V + st * C::TILE + sub * C::SUBT, &tmap_v,
-                      bar(C::QB_VFULL + st), sub * 64, map_coord(p.vperm[0], row, hk, b),
-                      map_coord(p.vperm[1], row, hk, b), map_coord(p.vperm[2], row, hk, b));
-        issued = n + 1;
+      mbar_arrive_expect_tx(bar(C::QB_QFULL), (uint32_t)(2 * C::TILE));
+      tma_tile<D>(sbase + C::Q_OFF_Q, &tmap_q, bar(C::QB_QFULL), p.qperm, (int)i0, h, b);
+      tma_tile<D>(sbase + C::Q_OFF_DO, &tmap_do, bar(C::QB_QFULL), p.operm, (int)i0, h, b);
+      // K~ and V tiles of key tile n; K~(n) is released after dQ~(n), V(n) after dP(n)
+      int nk = 0, nv = 0;
+      bool live = true;
+      while (live && (nk < N || nv < N)) {
+        bool progressed = false;
+        if (nk < N && (nk < C::NSK || mbar_try_wait(bar(C::QB_KEMPTY + nk % C::NSK),
+                                                    (uint32_t)((nk / C::NSK - 1) & 1)))) {
+          const int st = nk % C::NSK;
+          mbar_arrive_expect_tx(bar(C::QB_KFULL + st), (uint32_t)C::TILE);
+          tma_tile<D>(sbase + C::Q_OFF_K + st * C::TILE, &tmap_k, bar(C::QB_KFULL + st), p.kperm,
+                      nk * 128, hk, b);
+          ++nk;
+          progressed = true;
+        }
+        if (nv < N && (nv < C::NSV || mbar_try_wait(bar(C::QB_VEMPTY + nv % C::NSV),
+                                                    (uint32_t)((nv / C::NSV - 1) & 1)))) {
+          const int st = nv % C::NSV;
+          mbar_arrive_expect_tx(bar(C::QB_VFULL + st), (uint32_t)C::TILE);
+          tma_tile<D>(sbase + C::Q_OFF_V + st * C::TILE, &tmap_v, bar(C::QB_VFULL + st), p.vperm,
+                      nv * 128, hk, b);
+          ++nv;
+          progressed = true;
+        }
+        if (!progressed) {
+          // both rings full: wait (bounded) for the release the MMA needs first
+          const bool k_next = nk < N && (nv >= N || nk <= nv);
+          const uint32_t eb = k_next ? bar(C::QB_KEMPTY + nk % C::NSK) : bar(C::QB_VEMPTY + nv % C::NSV);
+          const uint32_t ep = k_next ? (uint32_t)((nk / C::NSK - 1) & 1) : (uint32_t)((nv / C::NSV - 1) & 1);
+          live = wait_bar(eb, ep, ctl);
+        }
       }
-      wait_bar_drain(bar(C::QB_DOFULL), 0u);
-      if (*abort_flag)
-        for (int n = max(0, issued - C::NS); n < issued; ++n)
-          wait_bar_drain(bar(C::QB_VFULL + n % C::NS), (uint32_t)((n / C::NS) & 1));
+      wait_bar_drain(bar(C::QB_QFULL), 0u);
+      if (*abort_flag) {
+        for (int n = max(0, nk - C::NSK); n < nk; ++n)
+          wait_bar_drain(bar(C::QB_KFULL + n % C::NSK), (uint32_t)((n / C::NSK) & 1));
+        for (int n = max(0, nv - C::NSV); n < nv; ++n)
+          wait_bar_drain(bar(C::QB_VFULL + n % C::NSV), (uint32_t)((n / C::NSV) & 1));
+      }
     }
-  } else {
+  } else if (lane == 0) {
     // =================================================================== MMA
-    if (lane == 0) {
-      constexpr uint32_t ab = std::is_same<TIn, __nv_bfloat16>::value ? 1u : 0u;
-      constexpr uint32_t IDESC_S = idesc_f16(0u, 0u, 128);   // fp16 Q~ x K~^T
-      constexpr uint32_t IDESC_DP = idesc_f16(ab, 0u, 128);  // dO x V^T
-      constexpr uint32_t IDESC_DQ = idesc_f16(0u, 1u, D);    // dS x K~ (K~ MN-major)
-      constexpr uint32_t HI = sdesc_hi_sw128(1024);
-      const uint32_t q_lo = sdesc_lo(sbase + C::Q_OFF_Q, 16);
-      const uint32_t do_lo = sdesc_lo(sbase + C::Q_OFF_DO, 16);
-      const uint32_t k_lo0 = sdesc_lo(sbase + C::Q_OFF_K, 16);
-      const uint32_t v_lo0 = sdesc_lo(sbase + C::Q_OFF_V, 16);
-      const uint32_t kmn_lo0 = sdesc_lo(sbase + C::Q_OFF_K, C::SUBT);
-      bool ok = wait_bar(bar(C::QB_QFULL), 0u, ctl) && wait_bar(bar(C::QB_DOFULL), 0u, ctl);
-      for (int n = 0; ok && n < N; ++n) {
-        const int st = n % C::NS;
-        if (!wait_bar(bar(C::QB_KFULL + st), (uint32_t)((n / C::NS) & 1), ctl) ||
-            !wait_bar(bar(C::QB_VFULL + st), (uint32_t)((n / C::NS) & 1), ctl)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t so = (uint32_t)(st * C::TILE >> 4);
+    constexpr uint32_t ab = std::is_same<TIn, __nv_bfloat16>::value ? 1u : 0u;
+    constexpr uint32_t IDESC_S = idesc_f16(0u, 0u, 128);   // fp16 Q~ x K~^T
+    constexpr uint32_t IDESC_DP = idesc_f16(ab, 0u, 128);  // dO x V^T
+    constexpr uint32_t IDESC_DQ = idesc_f16(0u, 1u, D);    // dS x K~ (K~ MN-major)
+    constexpr uint32_t HI = sdesc_hi_sw128(1024);
+    const uint32_t q_lo = sdesc_lo(sbase + C::Q_OFF_Q, 16);
+    const uint32_t do_lo = sdesc_lo(sbase + C::Q_OFF_DO, 16);
+    const uint32_t k_lo0 = sdesc_lo(sbase + C::Q_OFF_K, 16);
+    const uint32_t v_lo0 = sdesc_lo(sbase + C::Q_OFF_V, 16);
+    const uint32_t kmn_lo0 = sdesc_lo(sbase + C::Q_OFF_K, C::SUBT);
+    bool ok = wait_bar(bar(C::QB_QFULL), 0u, ctl);
+    // dQ~ += dS(m) K~(m), A = dS packed in S slot m & 1 (keys 64..127 at +64)
+    auto issue_dq = [&](int mm) {
+      const int st = mm % C::NSK, sl = mm & 1;
+      const uint32_t so = (uint32_t)(st * C::TILE >> 4);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (uint32_t)(((kk >> 2) * C::SUBT + (kk & 3) * 32) >> 4);
-          mma_ss(tmem, sdesc_join(q_lo + off, HI), sdesc_join(k_lo0 + so + off, HI), IDESC_S,
-                 kk > 0 ? 1u : 0u);
-        }
-        tc_commit(bar(C::QB_SFULL));
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (uint32_t)(((kk >> 2) * C::SUBT + (kk & 3) * 32) >> 4);
-          mma_ss(tmem + 128u, sdesc_join(do_lo + off, HI), sdesc_join(v_lo0 + so + off, HI),
-                 IDESC_DP, kk > 0 ? 1u : 0u);
-        }
-        tc_commit(bar(C::QB_DPFULL));
-        if (!wait_bar(bar(C::QB_PFULL), (uint32_t)(n & 1), ctl)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // 16 keys per step
-          mma_ts(tmem + 256u, tmem + (uint32_t)(kk * 8),
-                 sdesc_join(kmn_lo0 + so + (uint32_t)(kk * 2048 >> 4), HI), IDESC_DQ,
-                 (n > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(bar(C::QB_KEMPTY + st));
-        tc_commit(bar(C::QB_VEMPTY + st));
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ts(tmem + 384u, tmem + (uint32_t)(128 * sl + (kk >> 2) * 64 + (kk & 3) * 8),
+               sdesc_join(kmn_lo0 + so + (uint32_t)(kk * 2048 >> 4), HI), IDESC_DQ,
+               (mm > 0 || kk > 0) ? 1u : 0u);
+      tc_commit(bar(C::QB_KEMPTY + st));
+    };
+    // Issue order S(n), dP(n), dQ~(n-1): the tensor core computes the next
+    // tile's S and dP while the threads turn this tile's into dS.
+    for (int n = 0; ok && n < N; ++n) {
+      const int stk = n % C::NSK, stv = n % C::NSV, sl = n & 1;
+      if (!wait_bar(bar(C::QB_KFULL + stk), (uint32_t)((n / C::NSK) & 1), ctl)) {
+        ok = false;
+        break;
       }
-      if (ok) tc_commit(bar(C::QB_ACC));
-      tc_commit(bar(C::QB_DONE));
-      wait_bar_drain(bar(C::QB_DONE), 0u);
+      tc_fence_after();
+      const uint32_t sok = (uint32_t)(stk * C::TILE >> 4), sov = (uint32_t)(stv * C::TILE >> 4);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (uint32_t)(((kk >> 2) * C::SUBT + (kk & 3) * 32) >> 4);
+        mma_ss(tmem + (uint32_t)(128 * sl), sdesc_join(q_lo + off, HI),
+               sdesc_join(k_lo0 + sok + off, HI), IDESC_S, kk > 0 ? 1u : 0u);
+      }
+      tc_commit(bar(C::QB_SFULL + sl));
+      if (!wait_bar(bar(C::QB_VFULL + stv), (uint32_t)((n / C::NSV) & 1), ctl) ||
+          (n >= 1 && !wait_bar(bar(C::QB_DPFREE), (uint32_t)((n - 1) & 1), ctl))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (uint32_t)(((kk >> 2) * C::SUBT + (kk & 3) * 32) >> 4);
+        mma_ss(tmem + 256u, sdesc_join(do_lo + off, HI), sdesc_join(v_lo0 + sov + off, HI),
+               IDESC_DP, kk > 0 ? 1u : 0u);
+      }
+      tc_commit(bar(C::QB_DPFULL));
+      tc_commit(bar(C::QB_VEMPTY + stv));
+      if (n >= 1) {
+        if (!wait_bar(bar(C::QB_PFULL + ((n - 1) & 1)), (uint32_t)(((n - 1) >> 1) & 1), ctl)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_dq(n - 1);
+      }
     }
+    if (ok && N > 0) {
+      ok = wait_bar(bar(C::QB_PFULL + ((N - 1) & 1)), (uint32_t)(((N - 1) >> 1) & 1), ctl);
+      if (ok) {
+        tc_fence_after();
+        issue_dq(N - 1);
+        tc_commit(bar(C::QB_ACC));
+      }
+    }
+    tc_commit(bar(C::QB_DONE));
+    wait_bar_drain(bar(C::QB_DONE), 0u);
   }
 
   tc_fence_before();
@@ -694,7 +798,7 @@ EncodeTiledFn encode_fn() {
 // last); box 64 head-dim elements x 128 rows, 128-byte swizzle; rows past S
 // read as zero.
 cudaError_t make_rows_map(const void *base, int B, int H, int64_t S, int D, const int64_t st[3],
-                          ra_dtype dt, CUtensorMap *map, int perm[3]) {
+                          bool bf16, CUtensorMap *map, int perm[3]) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   struct Dim { uint64_t size, stride; int logical; };
@@ -718,16 +822,30 @@ cudaError_t make_rows_map(const void *base, int B, int H, int64_t S, int D, cons
     if (d[i].logical == 0) box[1 + i] = 128;
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUtensorMapDataType t =
-      dt == RA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+      bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const CUresult r = enc(map, t, 4, const_cast<void *>(base), gdim, gstride, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+template <typename TIn>
+cudaError_t rotate_f16(const void *x, int B, int H, int64_t S, int D, const int64_t st[3],
+                       int64_t pos0, __half *out, const AttnArgs &f, cudaStream_t s) {
+  const int64_t n = (int64_t)B * H * S * (D / 8);
+  if (n == 0) return cudaSuccess;
+  int64_t blocks = (n + 255) / 256;
+  const int64_t cap = (int64_t)sm_count_current() * 16;
+  if (blocks > cap) blocks = cap;
+  bwd_rotate_f16_kernel<TIn><<<(unsigned)blocks, 256, 0, s>>>(
+      static_cast<const TIn *>(x), H, S, D, st[0], st[1], st[2], pos0, out, f.apply_rope,
+      f.rot_dim, f.layout, f.cos_t, f.sin_t, n);
+  note_launch("bwd_rotate_f16_kernel");
+  return cudaGetLastError();
+}
+
 template <int D, typename TIn>
-cudaError_t launch_typed(const CUtensorMap &mv, const CUtensorMap &mdo, const BwdTcParams &p,
-                         cudaStream_t s) {
+cudaError_t launch_typed(const CUtensorMap (&maps)[4], const BwdTcParams &p, cudaStream_t s) {
   using C = BCfg<D>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
@@ -742,11 +860,13 @@ cudaError_t launch_typed(const CUtensorMap &mv, const CUtensorMap &mdo, const Bw
   const int64_t gk = (int64_t)p.n_kt * p.B * p.Hkv;
   const int64_t gq = (int64_t)p.n_qt * p.B * p.Hq;
   if (gk > 0x7fffffff || gq > 0x7fffffff) return cudaErrorInvalidConfiguration;
-  bwd_dkdv_tc_kernel<D, TIn><<<(unsigned)gk, kThreads, C::K_SMEM, s>>>(mv, mdo, p);
+  bwd_dkdv_tc_kernel<D, TIn><<<(unsigned)gk, kThreads, C::K_SMEM, s>>>(maps[0], maps[1], maps[2],
+                                                                       maps[3], p);
   note_launch("bwd_dkdv_tc_kernel");
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || gq == 0) return e;
-  bwd_dq_tc_kernel<D, TIn><<<(unsigned)gq, kThreads, C::Q_SMEM, s>>>(mv, mdo, p);
+  bwd_dq_tc_kernel<D, TIn><<<(unsigned)gq, kThreads, C::Q_SMEM, s>>>(maps[0], maps[1], maps[2],
+                                                                     maps[3], p);
   note_launch("bwd_dq_tc_kernel");
   return cudaGetLastError();
 }
@@ -756,21 +876,41 @@ cudaError_t launch_typed(const CUtensorMap &mv, const CUtensorMap &mdo, const Bw
 cudaError_t launch_attn_bwd_tc(const BwdArgs &a, cudaStream_t s) {
   const AttnArgs &f = a.f;
   if (f.D != 64 && f.D != 128) return cudaErrorNotSupported;
+  const bool bf = f.dt == RA_BF16;
+  // rotated fp16 copies of Q and K (contiguous [B][H][S][D]) in the workspace
+  const int64_t cq[3] = {(int64_t)f.Hq * f.Sq * f.D, f.Sq * f.D, f.D};
+  const int64_t ck[3] = {(int64_t)f.Hkv * f.Sk * f.D, f.Sk * f.D, f.D};
+  cudaError_t e = bf ? rotate_f16<__nv_bfloat16>(f.q, f.B, f.Hq, f.Sq, f.D, f.sq, f.kv_offset,
+                                                 static_cast<__half *>(a.qrot), f, s)
+                     : rotate_f16<__half>(f.q, f.B, f.Hq, f.Sq, f.D, f.sq, f.kv_offset,
+                                          static_cast<__half *>(a.qrot), f, s);
+  if (e == cudaSuccess)
+    e = bf ? rotate_f16<__nv_bfloat16>(f.k, f.B, f.Hkv, f.Sk, f.D, f.sk, 0,
+                                       static_cast<__half *>(a.krot), f, s)
+           : rotate_f16<__half>(f.k, f.B, f.Hkv, f.Sk, f.D, f.sk, 0,
+                                static_cast<__half *>(a.krot), f, s);
+  if (e != cudaSuccess) return e;
+
   BwdTcParams p{};
-  CUtensorMap mv, mdo;
-  cudaError_t e = make_rows_map(f.v, f.B, f.Hkv, f.Sk, f.D, f.sv, f.dt, &mv, p.vperm);
+  CUtensorMap maps[4];  // q~, k~, v, dO
+  e = make_rows_map(a.krot, f.B, f.Hkv, f.Sk, f.D, ck, false, &maps[1], p.kperm);
+  if (e == cudaSuccess) e = make_rows_map(f.v, f.B, f.Hkv, f.Sk, f.D, f.sv, bf, &maps[2], p.vperm);
   if (e != cudaSuccess) return e;
   if (f.Sq > 0) {
-    e = make_rows_map(a.dout, f.B, f.Hq, f.Sq, f.D, a.sdo, f.dt, &mdo, p.operm);
+    e = make_rows_map(a.qrot, f.B, f.Hq, f.Sq, f.D, cq, false, &maps[0], p.qperm);
+    if (e == cudaSuccess)
+      e = make_rows_map(a.dout, f.B, f.Hq, f.Sq, f.D, a.sdo, bf, &maps[3], p.operm);
     if (e != cudaSuccess) return e;
-  } else {
-    mdo = mv;  // never read: no query tiles
-    p.operm[0] = p.vperm[0]; p.operm[1] = p.vperm[1]; p.operm[2] = p.vperm[2];
+  } else {  // no query tiles: the maps are never read
+    maps[0] = maps[1];
+    maps[3] = maps[2];
+    for (int i = 0; i < 3; ++i) {
+      p.qperm[i] = p.kperm[i];
+      p.operm[i] = p.vperm[i];
+    }
   }
-  p.q = f.q; p.k = f.k; p.lse = a.lse; p.dsum = a.dsum;
+  p.lse = a.lse; p.dsum = a.dsum;
   p.dq = a.dq; p.dk = a.dk; p.dv = a.dv;
-  p.sq0 = f.sq[0]; p.sq1 = f.sq[1]; p.sq2 = f.sq[2];
-  p.sk0 = f.sk[0]; p.sk1 = f.sk[1]; p.sk2 = f.sk[2];
   p.sdq0 = a.sdq[0]; p.sdq1 = a.sdq[1]; p.sdq2 = a.sdq[2];
   p.sdk0 = a.sdk[0]; p.sdk1 = a.sdk[1]; p.sdk2 = a.sdk[2];
   p.sdv0 = a.sdv[0]; p.sdv1 = a.sdv[1]; p.sdv2 = a.sdv[2];
@@ -779,14 +919,13 @@ cudaError_t launch_attn_bwd_tc(const BwdArgs &a, cudaStream_t s) {
   p.n_qt = (int)((f.Sq + 127) / 128);
   p.n_kt = (int)((f.Sk + 127) / 128);
   p.apply_rope = f.apply_rope; p.rot_dim = f.rot_dim; p.layout = f.layout;
-  p.cos_t = f.cos_t; p.sin_t = f.sin_t; p.table_rows = f.table_rows;
+  p.cos_t = f.cos_t; p.sin_t = f.sin_t;
   p.scale = f.scale;
   p.scale_log2 = (float)((double)f.scale * 1.4426950408889634);
   p.status = f.status;
-  const bool bf = f.dt == RA_BF16;
   if (f.D == 64)
-    return bf ? launch_typed<64, __nv_bfloat16>(mv, mdo, p, s) : launch_typed<64, __half>(mv, mdo, p, s);
-  return bf ? launch_typed<128, __nv_bfloat16>(mv, mdo, p, s) : launch_typed<128, __half>(mv, mdo, p, s);
+    return bf ? launch_typed<64, __nv_bfloat16>(maps, p, s) : launch_typed<64, __half>(maps, p, s);
+  return bf ? launch_typed<128, __nv_bfloat16>(maps, p, s) : launch_typed<128, __half>(maps, p, s);
 }
 
 }  // namespace ra

@@ -114,7 +114,15 @@ struct BwdArgs {
   void *dq, *dk, *dv;
   int64_t sod[3], sdo[3], sdq[3], sdk[3], sdv[3];
   float *dsum;  // workspace: fp32 [B][Hq][Sq]
+  void *qrot, *krot;  // workspace (16-bit inputs): rotated fp16 Q [B][Hq][Sq][D], K [B][Hkv][Sk][D]
 };
+// Workspace layout of attn_bwd_causal_rope: byte offsets of the rotated Q
+// and K copies (0 when unused) and the total size.
+struct BwdWorkspace {
+  size_t qrot_off, krot_off, bytes;
+};
+bool plan_bwd_workspace(ra_dtype dt, int B, int Hq, int Hkv, int64_t Sq, int64_t Sk, int D,
+                        BwdWorkspace *w);
 
 cudaError_t launch_table_build(const TableArgs &a, cudaStream_t s);
 // D_i = <dO_i, O_i> into a.dsum (any dtype).

@@ -256,3 +256,16 @@ def test_decode_noalloc_rejections(L):
     assert call(512, 64, 8, 131072) == UNSUPPORTED
     assert call(2, 3, 2, 32) == INVALID      # Hq % Hkv
     assert call(2, 4, 2, 0) == INVALID       # max_kv_len
+
+
+def test_backward_workspace_size(L):
+    """D_i row terms always; fp16 rotated Q and K copies for 16-bit inputs."""
+    L.attn_bwd_workspace_size.restype = ctypes.c_size_t
+    up = lambda x: (x + 255) // 256 * 256
+    B, Hq, Hkv, Sq, Sk, D = 2, 8, 2, 100, 300, 128
+    assert L.attn_bwd_workspace_size(0, B, Hq, Hkv, ctypes.c_int64(Sq), ctypes.c_int64(Sk), D) == \
+        up(B * Hq * Sq * 4)
+    assert L.attn_bwd_workspace_size(1, B, Hq, Hkv, ctypes.c_int64(Sq), ctypes.c_int64(Sk), D) == \
+        up(B * Hq * Sq * 4) + up(B * Hq * Sq * D * 2) + up(B * Hkv * Sk * D * 2)
+    assert L.attn_bwd_workspace_size(7, B, Hq, Hkv, ctypes.c_int64(Sq), ctypes.c_int64(Sk), D) == \
+        ctypes.c_size_t(-1).value
