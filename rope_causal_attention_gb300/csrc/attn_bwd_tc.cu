@@ -604,22 +604,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       // key column c is admissible iff c <= lim
       const int64_t lim = min(qpos, p.Sk - 1) - jt;
       const uint32_t sbase_t = lanes + (uint32_t)(128 * sl);
+      uint32_t sr[64];
+      tmem_ld64(sbase_t + (uint32_t)(64 * hf), sr);
 #pragma unroll
       for (int bt = 0; bt < 2; ++bt) {
         const int c0 = 64 * hf + 32 * bt;  // key columns [c0, c0 + 32)
-        uint32_t sr[32];
-        tmem_ld32(sbase_t + (uint32_t)c0, sr);
         uint32_t pd[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float p0 = ex2(fmaf(__uint_as_float(sr[e]), sl2, -lse2));
-          float p1 = ex2(fmaf(__uint_as_float(sr[e + 1]), sl2, -lse2));
+          const int x = 32 * bt + e;
+          float p0 = ex2(fmaf(__uint_as_float(sr[x]), sl2, -lse2));
+          float p1 = ex2(fmaf(__uint_as_float(sr[x + 1]), sl2, -lse2));
           if (straddle) {
             if (c0 + e > lim) p0 = 0.f;
             if (c0 + e + 1 > lim) p1 = 0.f;
           }
-          pd[e >> 1] = f16x2(p0 * (__uint_as_float(dr[32 * bt + e]) - dsum),
-                             p1 * (__uint_as_float(dr[32 * bt + e + 1]) - dsum));
+          pd[e >> 1] = f16x2(p0 * (__uint_as_float(dr[x]) - dsum),
+                             p1 * (__uint_as_float(dr[x + 1]) - dsum));
         }
         // packed into columns this warp has already read: [64 hf + 16 bt, +16)
         tmem_st16(sbase_t + (uint32_t)(64 * hf + 16 * bt), pd);
