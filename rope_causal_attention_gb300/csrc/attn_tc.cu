@@ -80,7 +80,8 @@ struct TcCfg {
   static constexpr int B_PFULL = 4 + 4 * NS;
   static constexpr int B_OFULL = 6 + 4 * NS;
   static constexpr int B_DONE = 8 + 4 * NS;
-  static constexpr int NBAR = 9 + 4 * NS;
+  static constexpr int B_KRAW = 9 + 4 * NS;  // raw K tile landed (TMA), per stage
+  static constexpr int NBAR = 9 + 5 * NS;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;  // slack to align the base to 1024
   // tensor-memory columns: S0 | S1 | O0 | O1
@@ -100,6 +101,7 @@ struct TcParams {
   int64_t table_rows;
   float scale_log2;
   int vperm[3];  // tensor-map dims 1..3 -> logical coordinate (0 key row, 1 kv head, 2 batch)
+  int kperm[3];  // the same for the K map
   int *status;
   int withhold_v0;  // failure-detection test: never load V tile 0 (see launch_attn_tc)
 };
@@ -389,31 +391,144 @@ __device__ __forceinline__ void rotate_tile_full(const TIn *rows, int64_t row_st
   full_rot_store<D, TIn, LAYOUT>(raw, cb, sb, cst, sst, tile, t);
 }
 
-// K tiles of the whole key loop: the next tile's rows are loaded into
-// registers before waiting for its shared-memory stage to be released.
+// A raw K tile staged by TMA (128-byte swizzle, the operand layout) is
+// rotated in place, row by row: each of the thread's 16-byte chunks is read,
+// rotated (cos/sin advanced by angle addition as in full_rot_store) and
+// rewritten as fp16 at the position it was loaded from.
+template <int D, typename TIn, int LAYOUT>
+__device__ __forceinline__ void full_rot_inplace(uint8_t *tile, int t,
+                                                 float2 (&cb)[FullRot<D, LAYOUT>::NG],
+                                                 float2 (&sb)[FullRot<D, LAYOUT>::NG],
+                                                 const float2 (&cst)[FullRot<D, LAYOUT>::NG],
+                                                 const float2 (&sst)[FullRot<D, LAYOUT>::NG]) {
+  using F = FullRot<D, LAYOUT>;
+  const int c = t % F::CH, r0 = (t / F::CH) * F::RPG;
+  const int ch = (LAYOUT == RA_NEOX) ? c + D / 16 : c;  // chunk of the high members
+#pragma unroll 1
+  for (int r = 0; r < F::RPG; ++r) {
+    const int row = r0 + r;
+    uint4 raw[1][F::LD];
+    raw[0][0] = *reinterpret_cast<const uint4 *>(tile + (c >> 3) * 16384 + row * 128 +
+                                                 (((c & 7) ^ (row & 7)) << 4));
+    if (F::LD == 2)
+      raw[0][F::LD - 1] = *reinterpret_cast<const uint4 *>(tile + (ch >> 3) * 16384 + row * 128 +
+                                                           (((ch & 7) ^ (row & 7)) << 4));
+    uint32_t olo[4], ohi[4];
+#pragma unroll
+    for (int j = 0; j < F::NG; ++j) {
+      float2 L, H;
+      if (LAYOUT == RA_NEOX) {
+        L = unpack2<TIn>(w_of(raw[0][0], j));
+        H = unpack2<TIn>(w_of(raw[0][1], j));
+      } else {
+        const float2 u = unpack2<TIn>(w_of(raw[0][0], 2 * j));
+        const float2 v = unpack2<TIn>(w_of(raw[0][0], 2 * j + 1));
+        L = make_float2(u.x, v.x);
+        H = make_float2(u.y, v.y);
+      }
+      const float2 lc = __fmul2_rn(L, cb[j]);
+      const float2 hc = __fmul2_rn(H, cb[j]);
+      const float2 a = __ffma2_rn(make_float2(-H.x, -H.y), sb[j], lc);  // lo*c - hi*s
+      const float2 b = __ffma2_rn(L, sb[j], hc);                         // hi*c + lo*s
+      if (LAYOUT == RA_NEOX) {
+        olo[j] = f16x2(a.x, a.y);
+        ohi[j] = f16x2(b.x, b.y);
+      } else {
+        olo[2 * j] = f16x2(a.x, b.x);
+        olo[2 * j + 1] = f16x2(a.y, b.y);
+      }
+    }
+    *reinterpret_cast<uint4 *>(tile + (c >> 3) * 16384 + row * 128 + (((c & 7) ^ (row & 7)) << 4)) =
+        make_uint4(olo[0], olo[1], olo[2], olo[3]);
+    if (LAYOUT == RA_NEOX)
+      *reinterpret_cast<uint4 *>(tile + (ch >> 3) * 16384 + row * 128 + (((ch & 7) ^ (row & 7)) << 4)) =
+          make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
+#pragma unroll
+    for (int j = 0; j < F::NG; ++j) {
+      const float2 cn = __ffma2_rn(cb[j], cst[j], __fmul2_rn(make_float2(-sb[j].x, -sb[j].y), sst[j]));
+      sb[j] = __ffma2_rn(sb[j], cst[j], __fmul2_rn(cb[j], sst[j]));
+      cb[j] = cn;
+    }
+  }
+}
+
+// Chunk c of row `row` of a swizzled tile.
+__device__ __forceinline__ uint4 *tile_chunk(uint8_t *tile, int row, int c) {
+  return reinterpret_cast<uint4 *>(tile + (c >> 3) * 16384 + row * 128 + (((c & 7) ^ (row & 7)) << 4));
+}
+
+// One staged row rotated in place (any rot_dim the tensor-core path allows,
+// or no rotation): rotated pairs, then the tail converted to fp16.
+template <int D, typename TIn>
+__device__ __forceinline__ void rotate_row_inplace(uint8_t *tile, int row, int64_t pos,
+                                                   const TcParams &p) {
+  constexpr int NC = D / 8;
+  int done = 0;
+  if (p.apply_rope) {
+    const int half = p.rot_dim >> 1;
+    const float *cr = p.cos_t + pos * half;
+    const float *sr = p.sin_t + pos * half;
+    if (p.layout == RA_NEOX) {
+      const int hc = half >> 3;
+      for (int c = 0; c < hc; ++c) {
+        float lo[8], hi[8], cs[8], sn[8], a[8], b[8];
+        In16<TIn>::unpack(*tile_chunk(tile, row, c), lo);
+        In16<TIn>::unpack(*tile_chunk(tile, row, c + hc), hi);
+        ld_table4(cr + 8 * c, cs);
+        ld_table4(cr + 8 * c + 4, cs + 4);
+        ld_table4(sr + 8 * c, sn);
+        ld_table4(sr + 8 * c + 4, sn + 4);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          a[e] = lo[e] * cs[e] - hi[e] * sn[e];
+          b[e] = hi[e] * cs[e] + lo[e] * sn[e];
+        }
+        st_chunk(tile, row, c, a);
+        st_chunk(tile, row, c + hc, b);
+      }
+    } else {
+      for (int c = 0; c < (p.rot_dim >> 3); ++c) {
+        float x[8], cs[4], sn[4], y[8];
+        In16<TIn>::unpack(*tile_chunk(tile, row, c), x);
+        ld_table4(cr + 4 * c, cs);
+        ld_table4(sr + 4 * c, sn);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          y[2 * e] = x[2 * e] * cs[e] - x[2 * e + 1] * sn[e];
+          y[2 * e + 1] = x[2 * e + 1] * cs[e] + x[2 * e] * sn[e];
+        }
+        st_chunk(tile, row, c, y);
+      }
+    }
+    done = p.rot_dim >> 3;
+  }
+  if (!std::is_same<TIn, __half>::value) {  // the tail becomes fp16 too
+    for (int c = done; c < NC; ++c) {
+      float x[8];
+      In16<TIn>::unpack(*tile_chunk(tile, row, c), x);
+      st_chunk(tile, row, c, x);
+    }
+  }
+}
+
+// K tiles of the whole key loop: wait for the TMA-staged raw tile, rotate it
+// in place (cos/sin of the tile's rows computed before the wait), publish.
 template <int D, typename TIn, int LAYOUT, int NS>
-__device__ __forceinline__ void rotate_k_loop(const TIn *kbase, const TcParams &p, int N, int t,
-                                              uint8_t *k_tiles, uint32_t kfull0,
-                                              uint32_t kempty0, const Ctl &ctl) {
+__device__ __forceinline__ void rotate_k_loop(const TcParams &p, int N, int t, uint8_t *k_tiles,
+                                              uint32_t kraw0, uint32_t kfull0, const Ctl &ctl) {
   using F = FullRot<D, LAYOUT>;
   constexpr int TILE = 128 * D * 2;
-  uint4 raw[F::RPG][F::LD];
   float2 cb[F::NG], sb[F::NG], cst[F::NG], sst[F::NG];
   const int64_t r0 = (t / F::CH) * F::RPG;
   full_rot_table<D, LAYOUT>(p, p.table_rows > 1 ? 1 : 0, t, cst, sst);
-  if (N > 0) full_rot_load<D, TIn, LAYOUT>(kbase, p.sk2, p.Sk, t, raw);
   for (int n = 0; n < N; ++n) {
     const int st = n % NS;
     const int64_t j0 = (int64_t)n * 128;
     full_rot_table<D, LAYOUT>(p, r0 < p.Sk - j0 ? j0 + r0 : 0, t, cb, sb);
-    if (n >= NS && !wait_bar(kempty0 + 8u * st, (uint32_t)((n / NS - 1) & 1), ctl)) break;
-    full_rot_store<D, TIn, LAYOUT>(raw, cb, sb, cst, sst, k_tiles + st * TILE, t);
+    if (!wait_bar(kraw0 + 8u * st, (uint32_t)((n / NS) & 1), ctl)) break;
+    full_rot_inplace<D, TIn, LAYOUT>(k_tiles + st * TILE, t, cb, sb, cst, sst);
     fence_proxy_async_smem();
     mbar_arrive(kfull0 + 8u * st);
-    if (n + 1 < N) {
-      const int64_t j1 = j0 + 128;
-      full_rot_load<D, TIn, LAYOUT>(kbase + j1 * p.sk2, p.sk2, p.Sk - j1, t, raw);
-    }
   }
 }
 
@@ -437,7 +552,8 @@ constexpr float kTau = 8.0f;
 
 template <int D, typename TIn>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_v, const TcParams p) {
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                   const __grid_constant__ CUtensorMap tmap_v, const TcParams p) {
   using C = TcCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -472,6 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(C::B_QFULL + 0), 128);
     mbar_init(bar(C::B_QFULL + 1), 128);
     for (int i = 0; i < C::NS; ++i) {
+      mbar_init(bar(C::B_KRAW + i), 1);
       mbar_init(bar(C::B_KFULL + i), 128);
       mbar_init(bar(C::B_KEMPTY + i), 1);
       mbar_init(bar(C::B_VFULL + i), 1);
@@ -491,7 +608,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-  if (warp == kWarpTma && lane == 0) prefetch_tmap(&tmap_v);
+  if (warp == kWarpTma && lane == 0) {
+    prefetch_tmap(&tmap_k);
+    prefetch_tmap(&tmap_v);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -617,7 +737,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = threadIdx.x - kWarpRot * 32;
     const bool full_rot = p.apply_rope && p.rot_dim == D;
     const TIn *qbase = static_cast<const TIn *>(p.q);
-    const TIn *kbase = static_cast<const TIn *>(p.k) + b * p.sk0 + hk * p.sk1;
 #pragma unroll 1
     for (int s = 0; s < 2; ++s) {
       const bool act = s ? act1 : act0;
@@ -642,20 +761,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (full_rot) {
       if (p.layout == RA_NEOX)
-        rotate_k_loop<D, TIn, RA_NEOX, C::NS>(kbase, p, N, t, smem + C::OFF_K, bar(C::B_KFULL),
-                                             bar(C::B_KEMPTY), ctl);
+        rotate_k_loop<D, TIn, RA_NEOX, C::NS>(p, N, t, smem + C::OFF_K, bar(C::B_KRAW),
+                                             bar(C::B_KFULL), ctl);
       else
-        rotate_k_loop<D, TIn, RA_GPTJ, C::NS>(kbase, p, N, t, smem + C::OFF_K, bar(C::B_KFULL),
-                                             bar(C::B_KEMPTY), ctl);
+        rotate_k_loop<D, TIn, RA_GPTJ, C::NS>(p, N, t, smem + C::OFF_K, bar(C::B_KRAW),
+                                             bar(C::B_KFULL), ctl);
     } else {
       for (int n = 0; n < N; ++n) {
         const int st = n % C::NS;
-        if (n >= C::NS && !wait_bar(bar(C::B_KEMPTY + st), (uint32_t)((n / C::NS - 1) & 1), ctl))
-          break;
+        if (!wait_bar(bar(C::B_KRAW + st), (uint32_t)((n / C::NS) & 1), ctl)) break;
         const int64_t j = (int64_t)n * 128 + t;
-        const bool valid = j < p.Sk;
-        rotate_row<D, TIn>(kbase + (valid ? j : 0) * p.sk2, valid, j,
-                           smem + C::OFF_K + st * C::TILE, t, p);
+        if (j < p.Sk)  // rows past Sk were zero-filled by the TMA and stay zero
+          rotate_row_inplace<D, TIn>(smem + C::OFF_K + st * C::TILE, t, j, p);
         fence_proxy_async_smem();
         mbar_arrive(bar(C::B_KFULL + st));
       }
@@ -665,10 +782,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kWarpTma) {
       // ================================================================== TMA
       if (lane == 0) {
-        int issued = 0;
-        const int first_real = p.withhold_v0 ? 1 : 0;  // tiles below this are never loaded
+        int issued = 0, k_issued = 0;
+        const int first_real = p.withhold_v0 ? 1 : 0;  // V tiles below this are never loaded
         for (int n = 0; n < N; ++n) {
           const int st = n % C::NS;
+          // raw K tile n into its operand stage, once S(n - NS) has read the old one
+          if (n >= C::NS &&
+              !wait_bar(bar(C::B_KEMPTY + st), (uint32_t)((n / C::NS - 1) & 1), ctl))
+            break;
+          mbar_arrive_expect_tx(bar(C::B_KRAW + st), (uint32_t)C::TILE);
+          {
+            const int c1 = p.kperm[0] == 0 ? n * 128 : (p.kperm[0] == 1 ? hk : b);
+            const int c2 = p.kperm[1] == 0 ? n * 128 : (p.kperm[1] == 1 ? hk : b);
+            const int c3 = p.kperm[2] == 0 ? n * 128 : (p.kperm[2] == 1 ? hk : b);
+#pragma unroll
+            for (int sub = 0; sub < D / 64; ++sub)
+              tma_load_4d(sbase + C::OFF_K + st * C::TILE + sub * C::SUBT, &tmap_k,
+                          bar(C::B_KRAW + st), sub * 64, c1, c2, c3);
+          }
+          k_issued = n + 1;
           if (n >= C::NS &&
               !wait_bar(bar(C::B_VEMPTY + st), (uint32_t)((n / C::NS - 1) & 1), ctl))
             break;
@@ -684,6 +816,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           issued = n + 1;
         }
         if (*abort_flag) {  // let copies already in flight land before the block exits
+          for (int n = max(0, k_issued - C::NS); n < k_issued; ++n)
+            wait_bar_drain(bar(C::B_KRAW + n % C::NS), (uint32_t)((n / C::NS) & 1));
           for (int n = max(first_real, issued - C::NS); n < issued; ++n)
             wait_bar_drain(bar(C::B_VFULL + n % C::NS), (uint32_t)((n / C::NS) & 1));
         }
@@ -791,17 +925,18 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// V as a 4-D tensor map: dim 0 = head dim (contiguous), dims 1..3 = key row,
-// kv head and batch ordered by increasing stride (size-1 dims last); the box
-// is 64 head-dim elements x 128 key rows (1 along the other dims), with the
-// 128-byte swizzle.
-cudaError_t make_v_map(const AttnArgs &a, CUtensorMap *map, int vperm[3]) {
+// K or V as a 4-D tensor map: dim 0 = head dim (contiguous), dims 1..3 = key
+// row, kv head and batch ordered by increasing stride (size-1 dims last); the
+// box is 64 head-dim elements x 128 key rows (1 along the other dims), with
+// the 128-byte swizzle; rows past Sk read as zero.
+cudaError_t make_kv_map(const AttnArgs &a, const void *base, const int64_t st[3],
+                        CUtensorMap *map, int perm[3]) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   struct Dim { uint64_t size, stride; int logical; };
-  Dim d[3] = {{(uint64_t)a.Sk, (uint64_t)a.sv[2] * 2, 0},
-              {(uint64_t)a.Hkv, (uint64_t)a.sv[1] * 2, 1},
-              {(uint64_t)a.B, (uint64_t)a.sv[0] * 2, 2}};
+  Dim d[3] = {{(uint64_t)a.Sk, (uint64_t)st[2] * 2, 0},
+              {(uint64_t)a.Hkv, (uint64_t)st[1] * 2, 1},
+              {(uint64_t)a.B, (uint64_t)st[0] * 2, 2}};
   std::stable_sort(d, d + 3, [](const Dim &x, const Dim &y) {
     if ((x.size == 1) != (y.size == 1)) return y.size == 1;
     return x.stride < y.stride;
@@ -810,7 +945,7 @@ cudaError_t make_v_map(const AttnArgs &a, CUtensorMap *map, int vperm[3]) {
   for (int i = 0; i < 3; ++i) {
     if (d[i].size == 1 || d[i].stride == 0) d[i].stride = (prev_extent + 15) & ~uint64_t(15);
     prev_extent = d[i].stride * d[i].size;
-    vperm[i] = d[i].logical;
+    perm[i] = d[i].logical;
   }
   const cuuint64_t gdim[4] = {(cuuint64_t)a.D, d[0].size, d[1].size, d[2].size};
   const cuuint64_t gstride[3] = {d[0].stride, d[1].stride, d[2].stride};
@@ -820,15 +955,15 @@ cudaError_t make_v_map(const AttnArgs &a, CUtensorMap *map, int vperm[3]) {
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUtensorMapDataType dt =
       a.dt == RA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  const CUresult r = enc(map, dt, 4, const_cast<void *>(a.v), gdim, gstride, box, estr,
+  const CUresult r = enc(map, dt, 4, const_cast<void *>(base), gdim, gstride, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 template <int D, typename TIn>
-cudaError_t launch_typed(const AttnArgs &a, const CUtensorMap &map, const TcParams &p,
-                         unsigned grid, cudaStream_t s) {
+cudaError_t launch_typed(const AttnArgs &a, const CUtensorMap &kmap, const CUtensorMap &vmap,
+                         const TcParams &p, unsigned grid, cudaStream_t s) {
   using C = TcCfg<D>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
@@ -842,7 +977,7 @@ cudaError_t launch_typed(const AttnArgs &a, const CUtensorMap &map, const TcPara
     if (attr_err == cudaSuccess && fa.numRegs != 128) attr_err = cudaErrorInvalidConfiguration;
   });
   if (attr_err != cudaSuccess) return attr_err;
-  attn_tc_kernel<D, TIn><<<grid, kThreads, C::SMEM, s>>>(map, p);
+  attn_tc_kernel<D, TIn><<<grid, kThreads, C::SMEM, s>>>(kmap, vmap, p);
   return cudaGetLastError();
 }
 
@@ -850,9 +985,10 @@ cudaError_t launch_typed(const AttnArgs &a, const CUtensorMap &map, const TcPara
 
 cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t s) {
   if (a.D != 64 && a.D != 128) return cudaErrorNotSupported;
-  CUtensorMap map;
+  CUtensorMap kmap, vmap;
   TcParams p{};
-  cudaError_t e = make_v_map(a, &map, p.vperm);
+  cudaError_t e = make_kv_map(a, a.k, a.sk, &kmap, p.kperm);
+  if (e == cudaSuccess) e = make_kv_map(a, a.v, a.sv, &vmap, p.vperm);
   if (e != cudaSuccess) return e;
   p.q = a.q; p.k = a.k; p.o = a.o; p.lse = a.lse;
   p.sq0 = a.sq[0]; p.sq1 = a.sq[1]; p.sq2 = a.sq[2];
@@ -881,10 +1017,10 @@ cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t s) {
   if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
   const bool bf = a.dt == RA_BF16;
   if (a.D == 64)
-    return bf ? launch_typed<64, __nv_bfloat16>(a, map, p, (unsigned)grid, s)
-              : launch_typed<64, __half>(a, map, p, (unsigned)grid, s);
-  return bf ? launch_typed<128, __nv_bfloat16>(a, map, p, (unsigned)grid, s)
-            : launch_typed<128, __half>(a, map, p, (unsigned)grid, s);
+    return bf ? launch_typed<64, __nv_bfloat16>(a, kmap, vmap, p, (unsigned)grid, s)
+              : launch_typed<64, __half>(a, kmap, vmap, p, (unsigned)grid, s);
+  return bf ? launch_typed<128, __nv_bfloat16>(a, kmap, vmap, p, (unsigned)grid, s)
+            : launch_typed<128, __half>(a, kmap, vmap, p, (unsigned)grid, s);
 }
 
 }  // namespace ra
