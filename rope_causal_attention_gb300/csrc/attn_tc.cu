@@ -96,6 +96,7 @@ struct TcParams {
   int64_t sq0, sq1, sq2, sk0, sk1, sk2, so0, so1, so2;
   int64_t Sq, Sk, kv_off;
   int Hq, G, n_units, units_per_b, n_qt, pack_heads;
+  int mirror;  // one-q-head blocks: slot 1 takes the mirrored query tile (see launch_attn_tc)
   int apply_rope, rot_dim, layout;
   const float *cos_t, *sin_t;
   int64_t table_rows;
@@ -567,18 +568,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- work item: (batch, head unit, query tile), heaviest (last) tiles first
+  // ---- work item: (batch, head unit, query tile pair).  Two heads of one
+  // kv group share a query tile; one head takes two 128-row tiles, either
+  // adjacent (heaviest pairs first) or tile qt with its mirror n - 1 - qt,
+  // which gives every block the same number of key-tile steps.
   const int bid = blockIdx.x;
-  const int qt = p.n_qt - 1 - bid / p.n_units;
+  const int qt = p.mirror ? bid / p.n_units : p.n_qt - 1 - bid / p.n_units;
   const int unit = bid % p.n_units;
   const int b = unit / p.units_per_b, hu = unit % p.units_per_b;
   const int h0 = p.pack_heads ? 2 * hu : hu;
   const int h1 = p.pack_heads ? 2 * hu + 1 : hu;
-  const int64_t m00 = p.pack_heads ? (int64_t)qt * 128 : (int64_t)qt * 256;
-  const int64_t m01 = p.pack_heads ? m00 : m00 + 128;
+  const int64_t n128 = (p.Sq + 127) / 128;
+  const int64_t m00 = p.pack_heads || p.mirror ? (int64_t)qt * 128 : (int64_t)qt * 256;
+  const int64_t m01 = p.pack_heads ? m00 : (p.mirror ? (n128 - 1 - qt) * 128 : m00 + 128);
   const int hk = h0 / p.G;
   const int nkt = (int)((p.Sk + 127) / 128);
-  const bool act0 = m00 < p.Sq, act1 = m01 < p.Sq;
+  const bool act0 = m00 < p.Sq, act1 = m01 < p.Sq && (!p.mirror || m01 > m00);
   const int nend0 = act0 ? (int)min((int64_t)nkt, (min(m00 + 127, p.Sq - 1) + p.kv_off) / 128 + 1) : 0;
   const int nend1 = act1 ? (int)min((int64_t)nkt, (min(m01 + 127, p.Sq - 1) + p.kv_off) / 128 + 1) : 0;
   const int N = max(nend0, nend1);
@@ -1000,6 +1005,12 @@ cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t s) {
   p.units_per_b = p.pack_heads ? a.Hq / 2 : a.Hq;
   p.n_units = a.B * p.units_per_b;
   p.n_qt = (int)(p.pack_heads ? (a.Sq + 127) / 128 : (a.Sq + 255) / 256);
+  // A grid that fits on the SMs at once ends with its longest block, so one
+  // head's tiles are paired as qt and its mirror: each block then runs
+  // n/2 key tiles with both slots busy and the rest with one, instead of the
+  // last adjacent pair running ~n tiles with both.  Larger grids keep the
+  // adjacent pairs, which share more K tiles, heaviest first.
+  p.mirror = (!p.pack_heads && (int64_t)p.n_qt * p.n_units <= sm_count_current()) ? 1 : 0;
   p.apply_rope = a.apply_rope; p.rot_dim = a.rot_dim; p.layout = a.layout;
   p.cos_t = a.cos_t; p.sin_t = a.sin_t; p.table_rows = a.table_rows;
   p.scale_log2 = (float)((double)a.scale * 1.4426950408889634);

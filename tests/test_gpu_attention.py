@@ -110,6 +110,13 @@ TC_CASES = [
     (torch.bfloat16, 1, 3, 1, 129, 1500, 64, 1371, GPTJ, None),
     (torch.float16, 1, 4, 2, 190, 190, 128, 0, NEOX, None),
     (torch.float16, 2, 2, 2, 65, 100, 64, 35, GPTJ, None),
+    # one q head per block, tiles paired with their mirror: odd and even
+    # tile counts, a position offset, a ragged last tile
+    (torch.bfloat16, 1, 3, 1, 700, 900, 64, 200, GPTJ, None),
+    (torch.bfloat16, 2, 2, 2, 640, 640, 128, 0, NEOX, None),
+    (torch.float16, 1, 1, 1, 1100, 1100, 128, 0, GPTJ, 64),
+    # more blocks than SMs: adjacent tile pairs
+    (torch.bfloat16, 1, 40, 40, 1000, 1000, 64, 0, NEOX, None),
 ]
 
 
