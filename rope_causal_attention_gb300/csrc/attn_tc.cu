@@ -81,7 +81,10 @@ struct TcCfg {
   static constexpr int B_OFULL = 6 + 4 * NS;
   static constexpr int B_DONE = 8 + 4 * NS;
   static constexpr int B_KRAW = 9 + 4 * NS;  // raw K tile landed (TMA), per stage
-  static constexpr int NBAR = 9 + 5 * NS;
+  static constexpr int B_MERGE = 9 + 5 * NS;  // split blocks: slot 1's row statistics stored
+  static constexpr int NBAR = 10 + 5 * NS;
+  // split blocks leave query buffer 1 unused; slot 1's (m, l) per row go there
+  static constexpr int OFF_STATS = OFF_Q + TILE;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;  // slack to align the base to 1024
   // tensor-memory columns: S0 | S1 | O0 | O1
@@ -96,7 +99,7 @@ struct TcParams {
   int64_t sq0, sq1, sq2, sk0, sk1, sk2, so0, so1, so2;
   int64_t Sq, Sk, kv_off;
   int Hq, G, n_units, units_per_b, n_qt, pack_heads;
-  int mirror;  // one-q-head blocks: slot 1 takes the mirrored query tile (see launch_attn_tc)
+  int split;  // one query tile per block, its key tiles shared out between the two slots
   int apply_rope, rot_dim, layout;
   const float *cos_t, *sin_t;
   int64_t table_rows;
@@ -111,6 +114,16 @@ struct Ctl {
   volatile int *abort;
   int *status;
 };
+
+// Split blocks: slot 0 takes key tiles [0, c0), slot 1 [c0, c0 + c1) with
+// c0 - c1 in {0, 1}.  Both run off one K/V stream whose entries alternate
+// slot 0, slot 1 while both have tiles left; slot 0's last tile may close it.
+__device__ __forceinline__ int split_entry(int slot, int i, int c1) {
+  return slot ? 2 * i + 1 : (i < c1 ? 2 * i : c1 + i);
+}
+__device__ __forceinline__ int split_tile(int e, int c0, int c1) {
+  return e < 2 * c1 ? ((e & 1) ? c0 + (e >> 1) : (e >> 1)) : e - c1;
+}
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl &c) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -393,9 +406,10 @@ __device__ __forceinline__ void rotate_tile_full(const TIn *rows, int64_t row_st
 }
 
 // A raw K tile staged by TMA (128-byte swizzle, the operand layout) is
-// rotated in place, row by row: each of the thread's 16-byte chunks is read,
-// rotated (cos/sin advanced by angle addition as in full_rot_store) and
-// rewritten as fp16 at the position it was loaded from.
+// rotated in place: the thread's 16-byte chunks of U rows are read together,
+// rotated (cos/sin advanced row to row by angle addition as in
+// full_rot_store) and rewritten as fp16 where they were loaded from.  U rows
+// in flight hide the shared-memory load latency of each batch.
 template <int D, typename TIn, int LAYOUT>
 __device__ __forceinline__ void full_rot_inplace(uint8_t *tile, int t,
                                                  float2 (&cb)[FullRot<D, LAYOUT>::NG],
@@ -403,52 +417,60 @@ __device__ __forceinline__ void full_rot_inplace(uint8_t *tile, int t,
                                                  const float2 (&cst)[FullRot<D, LAYOUT>::NG],
                                                  const float2 (&sst)[FullRot<D, LAYOUT>::NG]) {
   using F = FullRot<D, LAYOUT>;
+  constexpr int U = (F::LD == 2) ? 2 : 4;
+  static_assert(F::RPG % U == 0, "rows per thread must split into batches");
   const int c = t % F::CH, r0 = (t / F::CH) * F::RPG;
   const int ch = (LAYOUT == RA_NEOX) ? c + D / 16 : c;  // chunk of the high members
+  auto at = [&](int row, int k) {
+    return reinterpret_cast<uint4 *>(tile + (k >> 3) * 16384 + row * 128 + (((k & 7) ^ (row & 7)) << 4));
+  };
 #pragma unroll 1
-  for (int r = 0; r < F::RPG; ++r) {
-    const int row = r0 + r;
-    uint4 raw[1][F::LD];
-    raw[0][0] = *reinterpret_cast<const uint4 *>(tile + (c >> 3) * 16384 + row * 128 +
-                                                 (((c & 7) ^ (row & 7)) << 4));
-    if (F::LD == 2)
-      raw[0][F::LD - 1] = *reinterpret_cast<const uint4 *>(tile + (ch >> 3) * 16384 + row * 128 +
-                                                           (((ch & 7) ^ (row & 7)) << 4));
-    uint32_t olo[4], ohi[4];
+  for (int rb = 0; rb < F::RPG; rb += U) {
+    uint4 raw[U][F::LD];
 #pragma unroll
-    for (int j = 0; j < F::NG; ++j) {
-      float2 L, H;
-      if (LAYOUT == RA_NEOX) {
-        L = unpack2<TIn>(w_of(raw[0][0], j));
-        H = unpack2<TIn>(w_of(raw[0][1], j));
-      } else {
-        const float2 u = unpack2<TIn>(w_of(raw[0][0], 2 * j));
-        const float2 v = unpack2<TIn>(w_of(raw[0][0], 2 * j + 1));
-        L = make_float2(u.x, v.x);
-        H = make_float2(u.y, v.y);
+    for (int u = 0; u < U; ++u) {
+      raw[u][0] = *at(r0 + rb + u, c);
+      if (F::LD == 2) raw[u][F::LD - 1] = *at(r0 + rb + u, ch);
+    }
+    uint32_t olo[U][4], ohi[U][4];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+#pragma unroll
+      for (int j = 0; j < F::NG; ++j) {
+        float2 L, H;
+        if (LAYOUT == RA_NEOX) {
+          L = unpack2<TIn>(w_of(raw[u][0], j));
+          H = unpack2<TIn>(w_of(raw[u][F::LD - 1], j));
+        } else {
+          const float2 a = unpack2<TIn>(w_of(raw[u][0], 2 * j));
+          const float2 b = unpack2<TIn>(w_of(raw[u][0], 2 * j + 1));
+          L = make_float2(a.x, b.x);
+          H = make_float2(a.y, b.y);
+        }
+        const float2 lc = __fmul2_rn(L, cb[j]);
+        const float2 hc = __fmul2_rn(H, cb[j]);
+        const float2 a = __ffma2_rn(make_float2(-H.x, -H.y), sb[j], lc);  // lo*c - hi*s
+        const float2 b = __ffma2_rn(L, sb[j], hc);                         // hi*c + lo*s
+        if (LAYOUT == RA_NEOX) {
+          olo[u][j] = f16x2(a.x, a.y);
+          ohi[u][j] = f16x2(b.x, b.y);
+        } else {
+          olo[u][2 * j] = f16x2(a.x, b.x);
+          olo[u][2 * j + 1] = f16x2(a.y, b.y);
+        }
       }
-      const float2 lc = __fmul2_rn(L, cb[j]);
-      const float2 hc = __fmul2_rn(H, cb[j]);
-      const float2 a = __ffma2_rn(make_float2(-H.x, -H.y), sb[j], lc);  // lo*c - hi*s
-      const float2 b = __ffma2_rn(L, sb[j], hc);                         // hi*c + lo*s
-      if (LAYOUT == RA_NEOX) {
-        olo[j] = f16x2(a.x, a.y);
-        ohi[j] = f16x2(b.x, b.y);
-      } else {
-        olo[2 * j] = f16x2(a.x, b.x);
-        olo[2 * j + 1] = f16x2(a.y, b.y);
+#pragma unroll
+      for (int j = 0; j < F::NG; ++j) {
+        const float2 cn = __ffma2_rn(cb[j], cst[j], __fmul2_rn(make_float2(-sb[j].x, -sb[j].y), sst[j]));
+        sb[j] = __ffma2_rn(sb[j], cst[j], __fmul2_rn(cb[j], sst[j]));
+        cb[j] = cn;
       }
     }
-    *reinterpret_cast<uint4 *>(tile + (c >> 3) * 16384 + row * 128 + (((c & 7) ^ (row & 7)) << 4)) =
-        make_uint4(olo[0], olo[1], olo[2], olo[3]);
-    if (LAYOUT == RA_NEOX)
-      *reinterpret_cast<uint4 *>(tile + (ch >> 3) * 16384 + row * 128 + (((ch & 7) ^ (row & 7)) << 4)) =
-          make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
 #pragma unroll
-    for (int j = 0; j < F::NG; ++j) {
-      const float2 cn = __ffma2_rn(cb[j], cst[j], __fmul2_rn(make_float2(-sb[j].x, -sb[j].y), sst[j]));
-      sb[j] = __ffma2_rn(sb[j], cst[j], __fmul2_rn(cb[j], sst[j]));
-      cb[j] = cn;
+    for (int u = 0; u < U; ++u) {
+      *at(r0 + rb + u, c) = make_uint4(olo[u][0], olo[u][1], olo[u][2], olo[u][3]);
+      if (LAYOUT == RA_NEOX)
+        *at(r0 + rb + u, ch) = make_uint4(ohi[u][0], ohi[u][1], ohi[u][2], ohi[u][3]);
     }
   }
 }
@@ -515,8 +537,9 @@ __device__ __forceinline__ void rotate_row_inplace(uint8_t *tile, int row, int64
 // K tiles of the whole key loop: wait for the TMA-staged raw tile, rotate it
 // in place (cos/sin of the tile's rows computed before the wait), publish.
 template <int D, typename TIn, int LAYOUT, int NS>
-__device__ __forceinline__ void rotate_k_loop(const TcParams &p, int N, int t, uint8_t *k_tiles,
-                                              uint32_t kraw0, uint32_t kfull0, const Ctl &ctl) {
+__device__ __forceinline__ void rotate_k_loop(const TcParams &p, int N, int c0, int c1, int t,
+                                              uint8_t *k_tiles, uint32_t kraw0, uint32_t kfull0,
+                                              const Ctl &ctl) {
   using F = FullRot<D, LAYOUT>;
   constexpr int TILE = 128 * D * 2;
   float2 cb[F::NG], sb[F::NG], cst[F::NG], sst[F::NG];
@@ -524,7 +547,7 @@ __device__ __forceinline__ void rotate_k_loop(const TcParams &p, int N, int t, u
   full_rot_table<D, LAYOUT>(p, p.table_rows > 1 ? 1 : 0, t, cst, sst);
   for (int n = 0; n < N; ++n) {
     const int st = n % NS;
-    const int64_t j0 = (int64_t)n * 128;
+    const int64_t j0 = (int64_t)(p.split ? split_tile(n, c0, c1) : n) * 128;
     full_rot_table<D, LAYOUT>(p, r0 < p.Sk - j0 ? j0 + r0 : 0, t, cb, sb);
     if (!wait_bar(kraw0 + 8u * st, (uint32_t)((n / NS) & 1), ctl)) break;
     full_rot_inplace<D, TIn, LAYOUT>(k_tiles + st * TILE, t, cb, sb, cst, sst);
@@ -543,13 +566,14 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 // to 512, i.e. exactly the 512 threads x 128 registers the block launches
 // with; the host refuses to launch a build that did not allocate 128.
 constexpr uint32_t kRegSoftmax = 160;
-constexpr uint32_t kRegRotate = 144;
-constexpr uint32_t kRegCtrl = 48;
+constexpr uint32_t kRegRotate = 120;
+constexpr uint32_t kRegCtrl = 72;
 static_assert(2 * kRegSoftmax + kRegRotate + kRegCtrl == 4 * 128, "register split");
 
 // Lazy rescaling: the exponent reference moves only when the row max grows by
 // more than 2^kTau, so P <= 2^kTau and O/l are rescaled rarely.
 constexpr float kTau = 8.0f;
+constexpr float kMFloor = -1e30f;  // below any finite scaled score
 
 template <int D, typename TIn>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -568,25 +592,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- work item: (batch, head unit, query tile pair).  Two heads of one
-  // kv group share a query tile; one head takes two 128-row tiles, either
-  // adjacent (heaviest pairs first) or tile qt with its mirror n - 1 - qt,
-  // which gives every block the same number of key-tile steps.
+  // ---- work item, heaviest first: (batch, head unit, query tile).  Two
+  // heads of one kv group share a query tile, or one head takes two adjacent
+  // 128-row tiles, or (split) one head's tile has its key tiles shared out
+  // between the two slots.
   const int bid = blockIdx.x;
-  const int qt = p.mirror ? bid / p.n_units : p.n_qt - 1 - bid / p.n_units;
+  const int qt = p.n_qt - 1 - bid / p.n_units;
   const int unit = bid % p.n_units;
   const int b = unit / p.units_per_b, hu = unit % p.units_per_b;
   const int h0 = p.pack_heads ? 2 * hu : hu;
   const int h1 = p.pack_heads ? 2 * hu + 1 : hu;
-  const int64_t n128 = (p.Sq + 127) / 128;
-  const int64_t m00 = p.pack_heads || p.mirror ? (int64_t)qt * 128 : (int64_t)qt * 256;
-  const int64_t m01 = p.pack_heads ? m00 : (p.mirror ? (n128 - 1 - qt) * 128 : m00 + 128);
+  const int64_t m00 = p.pack_heads || p.split ? (int64_t)qt * 128 : (int64_t)qt * 256;
+  const int64_t m01 = p.pack_heads || p.split ? m00 : m00 + 128;
   const int hk = h0 / p.G;
   const int nkt = (int)((p.Sk + 127) / 128);
-  const bool act0 = m00 < p.Sq, act1 = m01 < p.Sq && (!p.mirror || m01 > m00);
-  const int nend0 = act0 ? (int)min((int64_t)nkt, (min(m00 + 127, p.Sq - 1) + p.kv_off) / 128 + 1) : 0;
-  const int nend1 = act1 ? (int)min((int64_t)nkt, (min(m01 + 127, p.Sq - 1) + p.kv_off) / 128 + 1) : 0;
-  const int N = max(nend0, nend1);
+  // key tiles each query tile reaches (causal tile skipping)
+  const int nq0 = m00 < p.Sq ? (int)min((int64_t)nkt, (min(m00 + 127, p.Sq - 1) + p.kv_off) / 128 + 1) : 0;
+  const int nq1 = m01 < p.Sq ? (int)min((int64_t)nkt, (min(m01 + 127, p.Sq - 1) + p.kv_off) / 128 + 1) : 0;
+  // steps of each slot; a split block's slot 1 starts at key tile kb1
+  const int nend0 = p.split ? (nq0 + 1) / 2 : nq0;
+  const int nend1 = p.split ? nq0 / 2 : nq1;
+  const int kb1 = p.split ? nend0 : 0;
+  const bool act0 = nend0 > 0, act1 = nend1 > 0;
+  const bool q1 = act1 && !p.split;  // slot 1 has a query tile of its own
+  const int N = p.split ? nq0 : max(nend0, nend1);  // K/V stream entries
+  auto ktile = [&](int e) { return p.split ? split_tile(e, nend0, nend1) : e; };
 
   // ---- set-up: barriers, tensor memory
   if (threadIdx.x == 0) {
@@ -605,6 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(C::B_OFULL + s), 1);
     }
     mbar_init(bar(C::B_DONE), 1);
+    mbar_init(bar(C::B_MERGE), 128);
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -635,16 +666,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nend = slot ? nend1 : nend0;
     const int64_t m0 = slot ? m01 : m00;
     const int hq = slot ? h1 : h0;
+    const int kb = slot ? kb1 : 0;  // first key tile of this slot
     if (act) {
       const int64_t i = m0 + t;
       const int64_t qpos = p.kv_off + i;
       const float sl2 = p.scale_log2;
-      float m_used = -INFINITY, l = 0.f;
+      // The exponent reference starts at a finite floor, not -inf: a split
+      // block's slot 1 can meet rows with no admissible key in a tile, whose
+      // scores are all -inf; their P is then 2^-inf = 0 rather than NaN.
+      float m_used = kMFloor, l = 0.f;
       bool ok = true;
       for (int n = 0; n < nend; ++n) {
         if (!wait_bar(bar(C::B_SFULL + slot), (uint32_t)(n & 1), ctl)) { ok = false; break; }
         tc_fence_after();
-        const int64_t j0 = (int64_t)n * 128;
+        const int64_t j0 = (int64_t)(kb + n) * 128;
         uint32_t r[128];
         tmem_ld128(tS, r);
         if ((j0 + 127 > m0 + p.kv_off) || (j0 + 127 >= p.Sk)) {
@@ -705,35 +740,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(bar(C::B_PFULL + slot));
       }
-      // ---- epilogue: O = u / l, LSE = ln 2 * (m + log2 l)
-      if (ok && wait_bar(bar(C::B_OFULL + slot), 0u, ctl)) {
+      // ---- epilogue: O = u / l, LSE = ln 2 * (m + log2 l).  In a split
+      // block slot 1 hands its row statistics to slot 0, which merges the two
+      // partial sums held in tensor memory: with m = max(m0, m1) and
+      // a_s = 2^(m_s - m), O = (a0 u0 + a1 u1) / (a0 l0 + a1 l1).
+      float2 *stats = reinterpret_cast<float2 *>(smem + C::OFF_STATS);
+      if (p.split && slot == 1) {
+        if (ok) {
+          stats[t] = make_float2(m_used, l);
+          mbar_arrive(bar(C::B_MERGE));
+        }
+      } else if (ok && wait_bar(bar(C::B_OFULL + slot), 0u, ctl) &&
+                 (!(p.split && act1) || (wait_bar(bar(C::B_MERGE), 0u, ctl) &&
+                                         wait_bar(bar(C::B_OFULL + 1), 0u, ctl)))) {
         tc_fence_after();
-        const float inv_l = 1.f / l;
+        const bool merge = p.split && act1;
+        float mf = m_used, lf = l, a0 = 1.f, a1 = 0.f;
+        if (merge) {
+          const float2 o1 = stats[t];
+          mf = fmaxf(m_used, o1.x);
+          a0 = ex2(m_used - mf);
+          a1 = ex2(o1.x - mf);
+          lf = l * a0 + o1.y * a1;
+        }
+        const float inv_l = 1.f / lf;
+        const float c0 = a0 * inv_l, c1 = a1 * inv_l;
+        const uint32_t tO1 = tmem + lane_bits + C::o_col(1);
         const bool row_ok = i < p.Sq;
         TIn *dst = static_cast<TIn *>(p.o) + b * p.so0 + hq * p.so1 + i * p.so2;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
           tmem_ld32(tO + 32 * c, o);
+          if (merge) {
+            uint32_t u[32];
+            tmem_ld32(tO1 + 32 * c, u);
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              o[e] = __float_as_uint(fmaf(__uint_as_float(u[e]), c1, __uint_as_float(o[e]) * c0));
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * c0);
+          }
           if (row_ok) {
             uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * c);
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
-              uint4 u;
-              u.x = In16<TIn>::pack2(__uint_as_float(o[8 * g + 0]) * inv_l,
-                                     __uint_as_float(o[8 * g + 1]) * inv_l);
-              u.y = In16<TIn>::pack2(__uint_as_float(o[8 * g + 2]) * inv_l,
-                                     __uint_as_float(o[8 * g + 3]) * inv_l);
-              u.z = In16<TIn>::pack2(__uint_as_float(o[8 * g + 4]) * inv_l,
-                                     __uint_as_float(o[8 * g + 5]) * inv_l);
-              u.w = In16<TIn>::pack2(__uint_as_float(o[8 * g + 6]) * inv_l,
-                                     __uint_as_float(o[8 * g + 7]) * inv_l);
-              d4[g] = u;
+              uint4 v;
+              v.x = In16<TIn>::pack2(__uint_as_float(o[8 * g + 0]), __uint_as_float(o[8 * g + 1]));
+              v.y = In16<TIn>::pack2(__uint_as_float(o[8 * g + 2]), __uint_as_float(o[8 * g + 3]));
+              v.z = In16<TIn>::pack2(__uint_as_float(o[8 * g + 4]), __uint_as_float(o[8 * g + 5]));
+              v.w = In16<TIn>::pack2(__uint_as_float(o[8 * g + 6]), __uint_as_float(o[8 * g + 7]));
+              d4[g] = v;
             }
           }
         }
         if (row_ok && p.lse)
-          p.lse[((int64_t)b * p.Hq + hq) * p.Sq + i] = (m_used + log2f(l)) * 0.69314718055994531f;
+          p.lse[((int64_t)b * p.Hq + hq) * p.Sq + i] = (mf + log2f(lf)) * 0.69314718055994531f;
       }
     }
   } else if (warp < 12) {
@@ -744,8 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const TIn *qbase = static_cast<const TIn *>(p.q);
 #pragma unroll 1
     for (int s = 0; s < 2; ++s) {
-      const bool act = s ? act1 : act0;
-      if (!act) continue;
+      if (!(s ? q1 : act0)) continue;
       const int64_t m0 = s ? m01 : m00;
       const int hq = s ? h1 : h0;
       uint8_t *qtile = smem + C::OFF_Q + s * C::TILE;
@@ -766,16 +828,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (full_rot) {
       if (p.layout == RA_NEOX)
-        rotate_k_loop<D, TIn, RA_NEOX, C::NS>(p, N, t, smem + C::OFF_K, bar(C::B_KRAW),
-                                             bar(C::B_KFULL), ctl);
+        rotate_k_loop<D, TIn, RA_NEOX, C::NS>(p, N, nend0, nend1, t, smem + C::OFF_K,
+                                             bar(C::B_KRAW), bar(C::B_KFULL), ctl);
       else
-        rotate_k_loop<D, TIn, RA_GPTJ, C::NS>(p, N, t, smem + C::OFF_K, bar(C::B_KRAW),
-                                             bar(C::B_KFULL), ctl);
+        rotate_k_loop<D, TIn, RA_GPTJ, C::NS>(p, N, nend0, nend1, t, smem + C::OFF_K,
+                                             bar(C::B_KRAW), bar(C::B_KFULL), ctl);
     } else {
       for (int n = 0; n < N; ++n) {
         const int st = n % C::NS;
         if (!wait_bar(bar(C::B_KRAW + st), (uint32_t)((n / C::NS) & 1), ctl)) break;
-        const int64_t j = (int64_t)n * 128 + t;
+        const int64_t j = (int64_t)ktile(n) * 128 + t;
         if (j < p.Sk)  // rows past Sk were zero-filled by the TMA and stay zero
           rotate_row_inplace<D, TIn>(smem + C::OFF_K + st * C::TILE, t, j, p);
         fence_proxy_async_smem();
@@ -795,11 +857,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (n >= C::NS &&
               !wait_bar(bar(C::B_KEMPTY + st), (uint32_t)((n / C::NS - 1) & 1), ctl))
             break;
+          const int kt = ktile(n);
           mbar_arrive_expect_tx(bar(C::B_KRAW + st), (uint32_t)C::TILE);
           {
-            const int c1 = p.kperm[0] == 0 ? n * 128 : (p.kperm[0] == 1 ? hk : b);
-            const int c2 = p.kperm[1] == 0 ? n * 128 : (p.kperm[1] == 1 ? hk : b);
-            const int c3 = p.kperm[2] == 0 ? n * 128 : (p.kperm[2] == 1 ? hk : b);
+            const int c1 = p.kperm[0] == 0 ? kt * 128 : (p.kperm[0] == 1 ? hk : b);
+            const int c2 = p.kperm[1] == 0 ? kt * 128 : (p.kperm[1] == 1 ? hk : b);
+            const int c3 = p.kperm[2] == 0 ? kt * 128 : (p.kperm[2] == 1 ? hk : b);
 #pragma unroll
             for (int sub = 0; sub < D / 64; ++sub)
               tma_load_4d(sbase + C::OFF_K + st * C::TILE + sub * C::SUBT, &tmap_k,
@@ -811,9 +874,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           if (n < first_real) continue;
           mbar_arrive_expect_tx(bar(C::B_VFULL + st), (uint32_t)C::TILE);
-          const int c1 = p.vperm[0] == 0 ? n * 128 : (p.vperm[0] == 1 ? hk : b);
-          const int c2 = p.vperm[1] == 0 ? n * 128 : (p.vperm[1] == 1 ? hk : b);
-          const int c3 = p.vperm[2] == 0 ? n * 128 : (p.vperm[2] == 1 ? hk : b);
+          const int c1 = p.vperm[0] == 0 ? kt * 128 : (p.vperm[0] == 1 ? hk : b);
+          const int c2 = p.vperm[1] == 0 ? kt * 128 : (p.vperm[1] == 1 ? hk : b);
+          const int c3 = p.vperm[2] == 0 ? kt * 128 : (p.vperm[2] == 1 ? hk : b);
 #pragma unroll
           for (int sub = 0; sub < D / 64; ++sub)
             tma_load_4d(sbase + C::OFF_V + st * C::TILE + sub * C::SUBT, &tmap_v,
@@ -840,7 +903,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t k_lo0 = sdesc_lo(sbase + C::OFF_K, 16);
         const uint32_t v_lo0 = sdesc_lo(sbase + C::OFF_V, C::SUBT);
         auto mma_s = [&](int s, int st) {
-          const uint32_t qlo = q_lo0 + (uint32_t)(s * C::TILE >> 4);
+          const uint32_t qlo = q_lo0 + (uint32_t)((p.split ? 0 : s) * C::TILE >> 4);
           const uint32_t klo = k_lo0 + (uint32_t)(st * C::TILE >> 4);
           const uint32_t dS = tmem + C::s_col(s);
 #pragma unroll
@@ -860,42 +923,81 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         auto part = [&](int s, int n) { return n < (s ? nend1 : nend0); };
         bool ok = true;
-        if (act0) ok = wait_bar(bar(C::B_QFULL + 0), 0u, ctl);
-        if (ok && act1) ok = wait_bar(bar(C::B_QFULL + 1), 0u, ctl);
-        if (ok && N > 0) ok = wait_bar(bar(C::B_KFULL + 0), 0u, ctl);
-        if (ok && N > 0) {
-          for (int s = 0; s < 2; ++s)
-            if (part(s, 0)) {
-              mma_s(s, 0);
-              tc_commit(bar(C::B_SFULL + s));
-            }
-          tc_commit(bar(C::B_KEMPTY + 0));
-        }
-        for (int n = 0; ok && n < N; ++n) {
-          const int st = n % C::NS, nst = (n + 1) % C::NS;
-          if (!wait_bar(bar(C::B_VFULL + st), (uint32_t)((n / C::NS) & 1), ctl)) { ok = false; break; }
-          bool k_next = false;
-          for (int s = 0; s < 2; ++s) {
-            if (!part(s, n)) continue;
-            if (!wait_bar(bar(C::B_PFULL + s), (uint32_t)(n & 1), ctl)) { ok = false; break; }
-            tc_fence_after();
-            mma_pv(s, st, n > 0);
-            if (n == (s ? nend1 : nend0) - 1) tc_commit(bar(C::B_OFULL + s));
-            if (part(s, n + 1)) {
-              if (!k_next) {
-                if (!wait_bar(bar(C::B_KFULL + nst), (uint32_t)(((n + 1) / C::NS) & 1), ctl)) {
-                  ok = false;
-                  break;
-                }
-                k_next = true;
+        if (p.split) {
+          // both slots read query buffer 0; each K/V stream entry has one user
+          ok = wait_bar(bar(C::B_QFULL + 0), 0u, ctl);
+          for (int s = 0; ok && s < 2; ++s) {
+            if (!part(s, 0)) continue;
+            const int e = split_entry(s, 0, nend1), st = e % C::NS;
+            if (!wait_bar(bar(C::B_KFULL + st), (uint32_t)((e / C::NS) & 1), ctl)) { ok = false; break; }
+            mma_s(s, st);
+            tc_commit(bar(C::B_SFULL + s));
+            tc_commit(bar(C::B_KEMPTY + st));
+          }
+          for (int n = 0; ok && n < nend0; ++n) {
+            for (int s = 0; s < 2; ++s) {
+              if (!part(s, n)) continue;
+              const int e = split_entry(s, n, nend1), st = e % C::NS;
+              if (!wait_bar(bar(C::B_VFULL + st), (uint32_t)((e / C::NS) & 1), ctl) ||
+                  !wait_bar(bar(C::B_PFULL + s), (uint32_t)(n & 1), ctl)) {
+                ok = false;
+                break;
               }
-              mma_s(s, nst);
+              tc_fence_after();
+              mma_pv(s, st, n > 0);
+              tc_commit(bar(C::B_VEMPTY + st));
+              if (!part(s, n + 1)) {
+                tc_commit(bar(C::B_OFULL + s));
+                continue;
+              }
+              const int e2 = split_entry(s, n + 1, nend1), st2 = e2 % C::NS;
+              if (!wait_bar(bar(C::B_KFULL + st2), (uint32_t)((e2 / C::NS) & 1), ctl)) {
+                ok = false;
+                break;
+              }
+              mma_s(s, st2);
               tc_commit(bar(C::B_SFULL + s));
+              tc_commit(bar(C::B_KEMPTY + st2));
             }
           }
-          if (!ok) break;
-          tc_commit(bar(C::B_VEMPTY + st));
-          if (k_next) tc_commit(bar(C::B_KEMPTY + nst));
+        } else {
+          if (act0) ok = wait_bar(bar(C::B_QFULL + 0), 0u, ctl);
+          if (ok && act1) ok = wait_bar(bar(C::B_QFULL + 1), 0u, ctl);
+          if (ok && N > 0) ok = wait_bar(bar(C::B_KFULL + 0), 0u, ctl);
+          if (ok && N > 0) {
+            for (int s = 0; s < 2; ++s)
+              if (part(s, 0)) {
+                mma_s(s, 0);
+                tc_commit(bar(C::B_SFULL + s));
+              }
+            tc_commit(bar(C::B_KEMPTY + 0));
+          }
+          for (int n = 0; ok && n < N; ++n) {
+            const int st = n % C::NS, nst = (n + 1) % C::NS;
+            if (!wait_bar(bar(C::B_VFULL + st), (uint32_t)((n / C::NS) & 1), ctl)) { ok = false; break; }
+            bool k_next = false;
+            for (int s = 0; s < 2; ++s) {
+              if (!part(s, n)) continue;
+              if (!wait_bar(bar(C::B_PFULL + s), (uint32_t)(n & 1), ctl)) { ok = false; break; }
+              tc_fence_after();
+              mma_pv(s, st, n > 0);
+              if (n == (s ? nend1 : nend0) - 1) tc_commit(bar(C::B_OFULL + s));
+              if (part(s, n + 1)) {
+                if (!k_next) {
+                  if (!wait_bar(bar(C::B_KFULL + nst), (uint32_t)(((n + 1) / C::NS) & 1), ctl)) {
+                    ok = false;
+                    break;
+                  }
+                  k_next = true;
+                }
+                mma_s(s, nst);
+                tc_commit(bar(C::B_SFULL + s));
+              }
+            }
+            if (!ok) break;
+            tc_commit(bar(C::B_VEMPTY + st));
+            if (k_next) tc_commit(bar(C::B_KEMPTY + nst));
+          }
         }
         // all issued MMAs complete before tensor memory is released
         tc_commit(bar(C::B_DONE));
@@ -1005,12 +1107,20 @@ cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t s) {
   p.units_per_b = p.pack_heads ? a.Hq / 2 : a.Hq;
   p.n_units = a.B * p.units_per_b;
   p.n_qt = (int)(p.pack_heads ? (a.Sq + 127) / 128 : (a.Sq + 255) / 256);
-  // A grid that fits on the SMs at once ends with its longest block, so one
-  // head's tiles are paired as qt and its mirror: each block then runs
-  // n/2 key tiles with both slots busy and the rest with one, instead of the
-  // last adjacent pair running ~n tiles with both.  Larger grids keep the
-  // adjacent pairs, which share more K tiles, heaviest first.
-  p.mirror = (!p.pack_heads && (int64_t)p.n_qt * p.n_units <= sm_count_current()) ? 1 : 0;
+  // A grid that fits on the SMs at once ends with its longest block, which
+  // runs every key tile of the last query tile.  Such grids give each block
+  // one query tile and share its key tiles out between the two slots (the
+  // two partial softmax sums merged in tensor memory), so the longest block
+  // runs about half as many.  Larger grids keep the pairs above, which share
+  // each K tile between two slots.
+  p.split = 0;
+  if ((a.Sq + 127) / 128 >= 2 && (int64_t)p.n_qt * p.n_units <= sm_count_current()) {
+    p.split = 1;
+    p.pack_heads = 0;
+    p.units_per_b = a.Hq;
+    p.n_units = a.B * a.Hq;
+    p.n_qt = (int)((a.Sq + 127) / 128);
+  }
   p.apply_rope = a.apply_rope; p.rot_dim = a.rot_dim; p.layout = a.layout;
   p.cos_t = a.cos_t; p.sin_t = a.sin_t; p.table_rows = a.table_rows;
   p.scale_log2 = (float)((double)a.scale * 1.4426950408889634);

@@ -110,13 +110,19 @@ TC_CASES = [
     (torch.bfloat16, 1, 3, 1, 129, 1500, 64, 1371, GPTJ, None),
     (torch.float16, 1, 4, 2, 190, 190, 128, 0, NEOX, None),
     (torch.float16, 2, 2, 2, 65, 100, 64, 35, GPTJ, None),
-    # one q head per block, tiles paired with their mirror: odd and even
-    # tile counts, a position offset, a ragged last tile
+    # grids that fit on the SMs: one query tile per block, its key tiles
+    # shared out between the two slots; odd and even tile counts, offsets,
+    # ragged tiles, partial rotation, and (off = 129) rows with no admissible
+    # key in slot 1's first tile
     (torch.bfloat16, 1, 3, 1, 700, 900, 64, 200, GPTJ, None),
     (torch.bfloat16, 2, 2, 2, 640, 640, 128, 0, NEOX, None),
     (torch.float16, 1, 1, 1, 1100, 1100, 128, 0, GPTJ, 64),
-    # more blocks than SMs: adjacent tile pairs
+    (torch.bfloat16, 1, 2, 2, 300, 429, 64, 129, GPTJ, None),
+    (torch.bfloat16, 1, 2, 1, 400, 400, 128, 0, NEOX, 64),
+    # more blocks than SMs: adjacent tile pairs (one q head) and q-head pairs
     (torch.bfloat16, 1, 40, 40, 1000, 1000, 64, 0, NEOX, None),
+    (torch.bfloat16, 2, 32, 8, 600, 600, 128, 0, NEOX, None),
+    (torch.float16, 1, 64, 16, 640, 640, 64, 0, GPTJ, None),
 ]
 
 
