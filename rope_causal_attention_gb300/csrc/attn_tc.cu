@@ -42,7 +42,6 @@
 #include <math.h>
 #include <stdlib.h>
 
-#include <algorithm>
 #include <mutex>
 #include <type_traits>
 
@@ -1013,59 +1012,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------- host
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void *ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  });
-  return fn;
-}
-
-// K or V as a 4-D tensor map: dim 0 = head dim (contiguous), dims 1..3 = key
-// row, kv head and batch ordered by increasing stride (size-1 dims last); the
-// box is 64 head-dim elements x 128 key rows (1 along the other dims), with
-// the 128-byte swizzle; rows past Sk read as zero.
+// K or V as a tensor map over (key row, kv head, batch): box 64 head-dim
+// elements x 128 key rows, 128-byte swizzle (the MMA operand layout).
 cudaError_t make_kv_map(const AttnArgs &a, const void *base, const int64_t st[3],
                         CUtensorMap *map, int perm[3]) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return cudaErrorNotSupported;
-  struct Dim { uint64_t size, stride; int logical; };
-  Dim d[3] = {{(uint64_t)a.Sk, (uint64_t)st[2] * 2, 0},
-              {(uint64_t)a.Hkv, (uint64_t)st[1] * 2, 1},
-              {(uint64_t)a.B, (uint64_t)st[0] * 2, 2}};
-  std::stable_sort(d, d + 3, [](const Dim &x, const Dim &y) {
-    if ((x.size == 1) != (y.size == 1)) return y.size == 1;
-    return x.stride < y.stride;
-  });
-  uint64_t prev_extent = (uint64_t)a.D * 2;
-  for (int i = 0; i < 3; ++i) {
-    if (d[i].size == 1 || d[i].stride == 0) d[i].stride = (prev_extent + 15) & ~uint64_t(15);
-    prev_extent = d[i].stride * d[i].size;
-    perm[i] = d[i].logical;
-  }
-  const cuuint64_t gdim[4] = {(cuuint64_t)a.D, d[0].size, d[1].size, d[2].size};
-  const cuuint64_t gstride[3] = {d[0].stride, d[1].stride, d[2].stride};
-  cuuint32_t box[4] = {64, 1, 1, 1};
-  for (int i = 0; i < 3; ++i)
-    if (d[i].logical == 0) box[1 + i] = 128;  // 128 key rows, whichever map dim holds them
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
-  const CUtensorMapDataType dt =
-      a.dt == RA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  const CUresult r = enc(map, dt, 4, const_cast<void *>(base), gdim, gstride, box, estr,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+  const int64_t size[3] = {a.Sk, a.Hkv, a.B}, stride[3] = {st[2], st[1], st[0]};
+  return make_row_tile_map(base, a.dt == RA_BF16, a.D, 3, size, stride, map, perm);
 }
 
 template <int D, typename TIn>

@@ -31,7 +31,6 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
-#include <algorithm>
 #include <mutex>
 #include <type_traits>
 
@@ -437,56 +436,16 @@ __global__ void __launch_bounds__(kThreads, 2)
 }
 
 // ------------------------------------------------------------------- host
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void *ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  });
-  return fn;
-}
-
-// A cache buffer as a 3-D tensor map: dim 0 = the 128 head dims
-// (contiguous), dims 1-2 = row and kv head ordered by increasing stride
-// (size-1 dims last); box 64 dims x 128 rows, 128-byte swizzle.  Rows past
-// the buffer read as zero.
+// A cache buffer as a tensor map over (row, kv head): box 64 of the 128
+// head dims x 128 rows, 128-byte swizzle; rows past the buffer read as zero.
 cudaError_t make_cache_map(void *base, int64_t rows, int Hkv, const int64_t strides[2],
                            ra_dtype dt, CUtensorMap *map, int perm[2]) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return cudaErrorNotSupported;
-  struct Dim { uint64_t size, stride; int logical; };
-  Dim d[2] = {{(uint64_t)rows, (uint64_t)strides[0] * 2, 0},
-              {(uint64_t)Hkv, (uint64_t)strides[1] * 2, 1}};
-  std::stable_sort(d, d + 2, [](const Dim &x, const Dim &y) {
-    if ((x.size == 1) != (y.size == 1)) return y.size == 1;
-    return x.stride < y.stride;
-  });
-  uint64_t prev_extent = 128 * 2;
-  for (int i = 0; i < 2; ++i) {
-    if (d[i].size == 1 || d[i].stride == 0) d[i].stride = (prev_extent + 15) & ~uint64_t(15);
-    prev_extent = d[i].stride * d[i].size;
-    perm[i] = d[i].logical;
-  }
-  const cuuint64_t gdim[3] = {128, d[0].size, d[1].size};
-  const cuuint64_t gstride[2] = {d[0].stride, d[1].stride};
-  const cuuint32_t box[3] = {64, d[0].logical == 0 ? 128u : 1u, d[1].logical == 0 ? 128u : 1u};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  const CUtensorMapDataType t =
-      dt == RA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  const CUresult r = enc(map, t, 3, base, gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+  const int64_t size[3] = {rows, Hkv, 1}, stride[3] = {strides[0], strides[1], 0};
+  int p3[3];
+  const cudaError_t e = make_row_tile_map(base, dt == RA_BF16, 128, 2, size, stride, map, p3);
+  perm[0] = p3[0];
+  perm[1] = p3[1];
+  return e;
 }
 
 template <typename TIn, int NPAD>

@@ -2,6 +2,7 @@
 // Not part of the C ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -136,6 +137,17 @@ cudaError_t launch_attn_decode(const DecodeArgs &a, cudaStream_t s);
 // has no variant for the case.
 cudaError_t launch_attn_decode_tc(const DecodeArgs &a, cudaStream_t s);
 int sm_count_current();
+
+// A 16-bit tensor (bf16 or fp16) whose rows of D elements are contiguous,
+// addressed by n_outer (1..3) further coordinates with the given sizes and
+// element strides; coordinate 0 is the row.  The tiled tensor map sorts them
+// by increasing stride (size-1 dims last) into map dims 1..n_outer, writes
+// perm[map dim - 1] = coordinate, and uses a box of 64 elements x 128 rows
+// (1 along the other dims) with the 128-byte swizzle; rows past the end read
+// as zero.  cudaErrorNotSupported without the driver's encoder.
+cudaError_t make_row_tile_map(const void *base, bool bf16, int D, int n_outer,
+                              const int64_t size[3], const int64_t stride[3], CUtensorMap *map,
+                              int perm[3]);
 cudaError_t launch_rope_apply(const RopeArgs &a, bool vectorized, cudaStream_t s);
 cudaError_t launch_attn_simt(const AttnArgs &a, cudaStream_t s);
 // Returns cudaErrorNotSupported when the tensor-core kernel has no variant
