@@ -564,9 +564,9 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 // Register shares after re-allocation (per thread).  The four warpgroups sum
 // to 512, i.e. exactly the 512 threads x 128 registers the block launches
 // with; the host refuses to launch a build that did not allocate 128.
-constexpr uint32_t kRegSoftmax = 160;
-constexpr uint32_t kRegRotate = 120;
-constexpr uint32_t kRegCtrl = 72;
+constexpr uint32_t kRegSoftmax = 168;
+constexpr uint32_t kRegRotate = 88;
+constexpr uint32_t kRegCtrl = 88;
 static_assert(2 * kRegSoftmax + kRegRotate + kRegCtrl == 4 * 128, "register split");
 
 // Lazy rescaling: the exponent reference moves only when the row max grows by
@@ -666,6 +666,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t m0 = slot ? m01 : m00;
     const int hq = slot ? h1 : h0;
     const int kb = slot ? kb1 : 0;  // first key tile of this slot
+    if (slot ? q1 : act0) {
+      // the slot's query tile, rotated once into its operand buffer while
+      // the rotation warpgroup starts on the K stream
+      const TIn *qbase = static_cast<const TIn *>(p.q);
+      uint8_t *qtile = smem + C::OFF_Q + slot * C::TILE;
+      if (p.apply_rope && p.rot_dim == D) {
+        const TIn *rows = qbase + b * p.sq0 + hq * p.sq1 + m0 * p.sq2;
+        if (p.layout == RA_NEOX)
+          rotate_tile_full<D, TIn, RA_NEOX>(rows, p.sq2, p.Sq - m0, p.kv_off + m0, qtile, t, p);
+        else
+          rotate_tile_full<D, TIn, RA_GPTJ>(rows, p.sq2, p.Sq - m0, p.kv_off + m0, qtile, t, p);
+      } else {
+        const int64_t i = m0 + t;
+        const bool valid = i < p.Sq;
+        const TIn *src = qbase + b * p.sq0 + hq * p.sq1 + (valid ? i : 0) * p.sq2;
+        rotate_row<D, TIn>(src, valid, p.kv_off + i, qtile, t, p);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bar(C::B_QFULL + slot));
+    }
     if (act) {
       const int64_t i = m0 + t;
       const int64_t qpos = p.kv_off + i;
@@ -802,30 +822,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // =============================================================== rotation
     setmaxnreg_to<128, kRegRotate>();
     const int t = threadIdx.x - kWarpRot * 32;
-    const bool full_rot = p.apply_rope && p.rot_dim == D;
-    const TIn *qbase = static_cast<const TIn *>(p.q);
-#pragma unroll 1
-    for (int s = 0; s < 2; ++s) {
-      if (!(s ? q1 : act0)) continue;
-      const int64_t m0 = s ? m01 : m00;
-      const int hq = s ? h1 : h0;
-      uint8_t *qtile = smem + C::OFF_Q + s * C::TILE;
-      if (full_rot) {
-        const TIn *rows = qbase + b * p.sq0 + hq * p.sq1 + m0 * p.sq2;
-        if (p.layout == RA_NEOX)
-          rotate_tile_full<D, TIn, RA_NEOX>(rows, p.sq2, p.Sq - m0, p.kv_off + m0, qtile, t, p);
-        else
-          rotate_tile_full<D, TIn, RA_GPTJ>(rows, p.sq2, p.Sq - m0, p.kv_off + m0, qtile, t, p);
-      } else {
-        const int64_t i = m0 + t;
-        const bool valid = i < p.Sq;
-        const TIn *src = qbase + b * p.sq0 + hq * p.sq1 + (valid ? i : 0) * p.sq2;
-        rotate_row<D, TIn>(src, valid, p.kv_off + i, qtile, t, p);
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(bar(C::B_QFULL + s));
-    }
-    if (full_rot) {
+    if (p.apply_rope && p.rot_dim == D) {
       if (p.layout == RA_NEOX)
         rotate_k_loop<D, TIn, RA_NEOX, C::NS>(p, N, nend0, nend1, t, smem + C::OFF_K,
                                              bar(C::B_KRAW), bar(C::B_KFULL), ctl);
