@@ -534,20 +534,31 @@ __device__ __forceinline__ void rotate_row_inplace(uint8_t *tile, int row, int64
 }
 
 // K tiles of the whole key loop: wait for the TMA-staged raw tile, rotate it
-// in place (cos/sin of the tile's rows computed before the wait), publish.
+// in place, publish.  The cos/sin of the tile's first rows are loaded one
+// entry ahead, so their latency overlaps the previous tile's wait and
+// rotation instead of stalling the rotation.
 template <int D, typename TIn, int LAYOUT, int NS>
 __device__ __forceinline__ void rotate_k_loop(const TcParams &p, int N, int c0, int c1, int t,
                                               uint8_t *k_tiles, uint32_t kraw0, uint32_t kfull0,
                                               const Ctl &ctl) {
   using F = FullRot<D, LAYOUT>;
   constexpr int TILE = 128 * D * 2;
-  float2 cb[F::NG], sb[F::NG], cst[F::NG], sst[F::NG];
+  float2 cb[F::NG], sb[F::NG], cn[F::NG], sn[F::NG], cst[F::NG], sst[F::NG];
   const int64_t r0 = (t / F::CH) * F::RPG;
+  auto row0 = [&](int n) {  // table row of the thread's first row in entry n
+    const int64_t j0 = (int64_t)(p.split ? split_tile(n, c0, c1) : n) * 128;
+    return r0 < p.Sk - j0 ? j0 + r0 : 0;
+  };
   full_rot_table<D, LAYOUT>(p, p.table_rows > 1 ? 1 : 0, t, cst, sst);
+  if (N > 0) full_rot_table<D, LAYOUT>(p, row0(0), t, cn, sn);
   for (int n = 0; n < N; ++n) {
     const int st = n % NS;
-    const int64_t j0 = (int64_t)(p.split ? split_tile(n, c0, c1) : n) * 128;
-    full_rot_table<D, LAYOUT>(p, r0 < p.Sk - j0 ? j0 + r0 : 0, t, cb, sb);
+#pragma unroll
+    for (int j = 0; j < F::NG; ++j) {
+      cb[j] = cn[j];
+      sb[j] = sn[j];
+    }
+    if (n + 1 < N) full_rot_table<D, LAYOUT>(p, row0(n + 1), t, cn, sn);
     if (!wait_bar(kraw0 + 8u * st, (uint32_t)((n / NS) & 1), ctl)) break;
     full_rot_inplace<D, TIn, LAYOUT>(k_tiles + st * TILE, t, cb, sb, cst, sst);
     fence_proxy_async_smem();
