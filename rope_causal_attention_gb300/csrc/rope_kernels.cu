@@ -70,13 +70,13 @@ __global__ void __launch_bounds__(512) rope_apply_vec_kernel(RopeKParams p) {
   constexpr int LD = (LAYOUT == RA_NEOX) ? 2 : 1;       // 16-byte loads per head
   const int s = threadIdx.x;
   const int hy = blockDim.y;  // heads of a token are h = threadIdx.y + k * hy, k < NH
+  const bool rot_slice = s < p.s_rot, tail_slice = !rot_slice && s < p.s_rot + p.s_tail;
+  const int i0 = s * NP;  // first pair index of a rotated slice
+  // NeoX: low-half and high-half pieces; GPT-J: whole pairs; tail: a copy
+  const int off0 = rot_slice ? ((LAYOUT == RA_NEOX) ? i0 : 2 * i0) : p.rot_dim + (s - p.s_rot) * V;
+  const int off1 = i0 + p.half;
   for (int64_t t = (int64_t)blockIdx.x * blockDim.z + threadIdx.z; t < p.T;
        t += (int64_t)gridDim.x * blockDim.z) {
-    const int64_t pos = load_position(p.positions, p.is64, t);
-    if (pos < 0 || pos >= p.table_rows) {
-      if (s == 0 && threadIdx.y == 0) record_status(p.status, RA_ERR_POSITION_RANGE);
-      continue;
-    }
     const T *src[NH];
     T *dst[NH];
     bool ok[NH];
@@ -91,18 +91,21 @@ __global__ void __launch_bounds__(512) rope_apply_vec_kernel(RopeKParams p) {
       dst[k] = static_cast<T *>(isq ? p.qo : p.ko) + t * (isq ? p.sqo_t : p.sko_t) +
                hh * (isq ? p.sqo_h : p.sko_h);
     }
-    if (s < p.s_rot) {
-      const int i0 = s * NP;  // first pair index of this slice
-      // NeoX: low-half and high-half pieces; GPT-J: whole pairs
-      const int off0 = (LAYOUT == RA_NEOX) ? i0 : 2 * i0;
-      const int off1 = i0 + p.half;
-      uint4 raw[NH][LD];
+    // the token's rows are read before its position, so that the position
+    // (and then the cos/sin row) is fetched while the rows are in flight
+    uint4 raw[NH][LD];
 #pragma unroll
-      for (int k = 0; k < NH; ++k) {
-        if (!ok[k]) continue;
-        raw[k][0] = *reinterpret_cast<const uint4 *>(src[k] + off0);
-        if (LD == 2) raw[k][LD - 1] = *reinterpret_cast<const uint4 *>(src[k] + off1);
-      }
+    for (int k = 0; k < NH; ++k) {
+      if (!ok[k] || !(rot_slice || tail_slice)) continue;
+      raw[k][0] = *reinterpret_cast<const uint4 *>(src[k] + off0);
+      if (LD == 2 && rot_slice) raw[k][LD - 1] = *reinterpret_cast<const uint4 *>(src[k] + off1);
+    }
+    const int64_t pos = load_position(p.positions, p.is64, t);
+    if (pos < 0 || pos >= p.table_rows) {
+      if (s == 0 && threadIdx.y == 0) record_status(p.status, RA_ERR_POSITION_RANGE);
+      continue;
+    }
+    if (rot_slice) {
       float c[NP], sn[NP];
       load_table<NP>(p.cos_t + pos * p.half + i0, c);
       load_table<NP>(p.sin_t + pos * p.half + i0, sn);
@@ -131,15 +134,10 @@ __global__ void __launch_bounds__(512) rope_apply_vec_kernel(RopeKParams p) {
           *reinterpret_cast<uint4 *>(dst[k] + off0) = pack16<T>(y);
         }
       }
-    } else if (s < p.s_rot + p.s_tail) {  // out of place: copy the unrotated tail
-      const int e0 = p.rot_dim + (s - p.s_rot) * V;
-      uint4 raw[NH];
+    } else if (tail_slice) {  // out of place: copy the unrotated tail
 #pragma unroll
       for (int k = 0; k < NH; ++k)
-        if (ok[k]) raw[k] = *reinterpret_cast<const uint4 *>(src[k] + e0);
-#pragma unroll
-      for (int k = 0; k < NH; ++k)
-        if (ok[k]) *reinterpret_cast<uint4 *>(dst[k] + e0) = raw[k];
+        if (ok[k]) *reinterpret_cast<uint4 *>(dst[k] + off0) = raw[k][0];
     }
   }
 }
@@ -182,12 +180,6 @@ __global__ void __launch_bounds__(256) rope_apply_scalar_kernel(RopeKParams p, i
   }
 }
 
-int sm_count() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
-  return n;
-}
 
 template <typename T>
 cudaError_t launch_vec(const RopeKParams &kp, ra_layout layout, cudaStream_t s) {
@@ -200,7 +192,7 @@ cudaError_t launch_vec(const RopeKParams &kp, ra_layout layout, cudaStream_t s) 
   if (tz < 1) tz = 1;
   if (tz > 64) tz = 64;
   const dim3 block(slices, hy, tz);
-  const int64_t max_grid = (int64_t)sm_count() * 64;
+  const int64_t max_grid = (int64_t)sm_count_current() * 64;
   const int64_t need = (kp.T + tz - 1) / tz;
   const unsigned grid = (unsigned)(need < max_grid ? need : max_grid);
   if (layout == RA_NEOX)
@@ -213,7 +205,7 @@ cudaError_t launch_vec(const RopeKParams &kp, ra_layout layout, cudaStream_t s) 
 template <typename T>
 cudaError_t launch_scalar(const RopeKParams &kp, ra_layout layout, int tail, cudaStream_t s) {
   const dim3 block(32, 8);
-  const int64_t max_grid = (int64_t)sm_count() * 64;
+  const int64_t max_grid = (int64_t)sm_count_current() * 64;
   const unsigned grid = (unsigned)(kp.T < max_grid ? kp.T : max_grid);
   rope_apply_scalar_kernel<T><<<grid, block, 0, s>>>(kp, (int)layout, tail);
   return cudaGetLastError();
@@ -227,7 +219,7 @@ cudaError_t launch_table_build(const TableArgs &a, cudaStream_t s) {
   const int64_t n = a.rows * half;
   if (n == 0) return cudaSuccess;
   int64_t blocks = (n + 255) / 256;
-  const int64_t cap = (int64_t)sm_count() * 32;
+  const int64_t cap = (int64_t)sm_count_current() * 32;
   if (blocks > cap) blocks = cap;
   rope_table_build_kernel<<<(unsigned)blocks, 256, 0, s>>>(a.cos_out, a.sin_out, a.rows, half,
                                                           a.base, F, a.pos_scale);

@@ -123,6 +123,7 @@ TC_CASES = [
     (torch.bfloat16, 1, 40, 40, 1000, 1000, 64, 0, NEOX, None),
     (torch.bfloat16, 2, 32, 8, 600, 600, 128, 0, NEOX, None),
     (torch.float16, 1, 64, 16, 640, 640, 64, 0, GPTJ, None),
+    (torch.bfloat16, 1, 20, 20, 2000, 2000, 128, 0, GPTJ, None),
 ]
 
 

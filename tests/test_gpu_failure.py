@@ -26,22 +26,26 @@ import __graft_entry__ as g
 g.build()
 import rope_causal_attention_gb300 as ra
 import workloads as wl
-q, k, v = [t.cuda() for t in wl.attn_qkv(1, 2, 1, 128, 256, 64, torch.bfloat16, 3)]
-cos, sin = ra.make_tables(256, 64, 10000.0)
-ra.attn_fwd_causal_rope(q, k, v, cos, sin, kv_offset=128)
+Sq, Sk = int(sys.argv[2]), int(sys.argv[3])
+q, k, v = [t.cuda() for t in wl.attn_qkv(1, 2, 1, Sq, Sk, 64, torch.bfloat16, 3)]
+cos, sin = ra.make_tables(Sk, 64, 10000.0)
+ra.attn_fwd_causal_rope(q, k, v, cos, sin, kv_offset=Sk - Sq)
 code = ra.ra_get_device_status()
 print("STATUS", code)
 import os
 os.environ.pop("RA_TEST_WITHHOLD_V_TILE0")
-o, lse = ra.attn_fwd_causal_rope(q, k, v, cos, sin, kv_offset=128)
+o, lse = ra.attn_fwd_causal_rope(q, k, v, cos, sin, kv_offset=Sk - Sq)
 print("AFTER", ra.ra_get_device_status(), bool(torch.isfinite(o.float()).all()))
 """
 
 
-def test_withheld_copy_times_out_cleanly():
+# one query tile (both slots of a block on it), and three tiles of a grid
+# that fits on the SMs (split blocks: the two slots share out the key tiles)
+@pytest.mark.parametrize("Sq,Sk", [(128, 256), (384, 512)])
+def test_withheld_copy_times_out_cleanly(Sq, Sk):
     env = dict(os.environ, RA_TEST_WITHHOLD_V_TILE0="1")
-    r = subprocess.run([sys.executable, "-c", CHILD, ROOT], env=env, capture_output=True,
-                       text=True, timeout=300)
+    r = subprocess.run([sys.executable, "-c", CHILD, ROOT, str(Sq), str(Sk)], env=env,
+                       capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = dict(l.split(" ", 1) for l in r.stdout.splitlines() if l.startswith(("STATUS", "AFTER")))
     assert lines["STATUS"].strip() == "-6"          # RA_ERR_DEVICE_TIMEOUT
