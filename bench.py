@@ -212,6 +212,8 @@ def run_reference(args, ws, rank):
 
 
 def attn_workload(args):
+    if args.attn_workload:
+        return next(w for w in wl.ALL_ATTN if w.name == args.attn_workload)
     if args.attn_sq:
         import dataclasses
         return dataclasses.replace(ATTN, Sq=args.attn_sq, Sk=args.attn_sq + ATTN.kv_offset,
@@ -691,6 +693,9 @@ def main():
     ap.add_argument("--attn-sq", type=int, default=0,
                     help="profiling aid: shrink the attention workload to this many new "
                          "queries (the 4096-row cached prefix is kept)")
+    ap.add_argument("--attn-workload", choices=[w.name for w in wl.ALL_ATTN], default=None,
+                    help="profiling aid (with --only attn): time this attention workload "
+                         "instead of the long-context one")
     ap.add_argument("--sweep", action="store_true",
                     help="report: time every attention workload (fp32, the GPT-J sweep, "
                          "long-context GQA) and both rope workloads, one JSON line each")
