@@ -7,10 +7,14 @@
 // rotated as it is staged in shared memory, online softmax with running max m,
 // denominator l and numerator u, output u / l, LSE = m + ln l.
 //
-// Layout: one warp per query row (lanes split the head dimension, D <= 256),
-// eight rows per block, key tiles of 32 rows staged (rotated) in shared
-// memory and shared by the eight warps.  Lane j of a warp holds the score of
-// key j of the tile, so the tile's softmax statistics are warp reductions.
+// Layout: one warp per query row (lanes split the head dimension for the
+// output, D <= 256), eight rows per block, key tiles of 32 rows staged and
+// rotated in shared memory (rows padded by one float, so 32 lanes reading 32
+// different rows at one column hit 32 banks) and shared by the eight warps.
+// Lane j of a warp computes the whole score of key j of the tile against the
+// warp's rotated query row (shared memory, read as a broadcast), so the
+// tile's softmax statistics are warp reductions.  Rotation is by pairs: one
+// cos/sin read per pair.
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -46,54 +50,42 @@ __device__ __forceinline__ float warp_max(float x) {
   return x;
 }
 
-// Rotated value of dim d of row x (fp32 values, length D) at position pos.
-__device__ __forceinline__ float rotated(const float *x, int d, int64_t pos, const SimtParams &p) {
-  if (!p.apply_rope || d >= p.rot_dim) return x[d];
+// Rotates pair i (< rot_dim / 2) of row x (fp32, any memory) in place at
+// position pos: NeoX pairs (i, i + rot_dim/2), GPT-J pairs (2i, 2i+1).
+__device__ __forceinline__ void rotate_pair(float *x, int i, int64_t pos, const SimtParams &p) {
   const int half = p.rot_dim >> 1;
-  int i, partner;
-  bool low;
-  if (p.layout == RA_NEOX) {
-    low = d < half;
-    i = low ? d : d - half;
-    partner = low ? d + half : d - half;
-  } else {
-    low = (d & 1) == 0;
-    i = d >> 1;
-    partner = low ? d + 1 : d - 1;
-  }
+  const int lo = p.layout == RA_NEOX ? i : 2 * i;
+  const int hi = p.layout == RA_NEOX ? i + half : 2 * i + 1;
   const float c = __ldg(p.cos_t + pos * half + i);
   const float s = __ldg(p.sin_t + pos * half + i);
-  return low ? x[d] * c - x[partner] * s : x[d] * c + x[partner] * s;
+  const float a = x[lo], b = x[hi];
+  x[lo] = a * c - b * s;
+  x[hi] = b * c + a * s;
 }
 
 __global__ void __launch_bounds__(kRows * 32) attn_simt_kernel(SimtParams p) {
   extern __shared__ float smem[];
-  const int D = p.D;
-  float *sK = smem;                      // [kTileK][D] rotated keys
-  float *sV = sK + kTileK * D;           // [kTileK][D]
-  float *sRaw = sV + kTileK * D;         // [kTileK][D] raw keys, then per-warp q rows
+  const int D = p.D, DP = D + 1;
+  float *sK = smem;                  // [kTileK][D + 1] rotated keys
+  float *sV = sK + kTileK * DP;      // [kTileK][D]
+  float *sQ = sV + kTileK * D;       // [kRows][D] rotated query rows
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y, b = blockIdx.z, hk = h / p.G;
   const int64_t i = (int64_t)blockIdx.x * kRows + warp;  // this warp's query row
   const bool row_ok = i < p.Sq;
   const int64_t qpos = p.kv_offset + i;
+  const int half = p.apply_rope ? p.rot_dim >> 1 : 0;  // rotated pairs per row
 
-  // ---- rotate this warp's query row once
-  float qr[kMaxPerLane];
+  // ---- this warp's query row, rotated once
+  float *qs = sQ + warp * D;
   {
-    float *xr = sRaw + warp * D;
-    if (row_ok) {
-      const float *src = p.q + b * p.sq[0] + h * p.sq[1] + i * p.sq[2];
-      for (int d = lane; d < D; d += 32) xr[d] = src[d];
-    }
+    const float *src = p.q + b * p.sq[0] + h * p.sq[1] + (row_ok ? i : 0) * p.sq[2];
+    for (int d = lane; d < D; d += 32) qs[d] = row_ok ? src[d] : 0.f;
     __syncwarp();
-#pragma unroll
-    for (int u = 0; u < kMaxPerLane; ++u) {
-      const int d = lane + 32 * u;
-      qr[u] = (row_ok && d < D) ? rotated(xr, d, qpos, p) : 0.f;
-    }
+    if (row_ok)
+      for (int e = lane; e < half; e += 32) rotate_pair(qs, e, qpos, p);
+    __syncwarp();
   }
-  __syncthreads();
 
   float m = -INFINITY, l = 0.f, acc[kMaxPerLane];
 #pragma unroll
@@ -106,7 +98,7 @@ __global__ void __launch_bounds__(kRows * 32) attn_simt_kernel(SimtParams p) {
 
   for (int64_t j0 = 0; j0 < kend; j0 += kTileK) {
     const int nk = (int)min((int64_t)kTileK, kend - j0);
-    // stage raw K and V
+    // stage raw K (padded rows) and V
     for (int e = threadIdx.x; e < kTileK * D; e += blockDim.x) {
       const int jj = e / D, d = e - jj * D;
       float kx = 0.f, vx = 0.f;
@@ -114,30 +106,31 @@ __global__ void __launch_bounds__(kRows * 32) attn_simt_kernel(SimtParams p) {
         kx = kb[(j0 + jj) * p.sk[2] + d];
         vx = vb[(j0 + jj) * p.sv[2] + d];
       }
-      sRaw[e] = kx;
+      sK[jj * DP + d] = kx;
       sV[e] = vx;
     }
     __syncthreads();
-    // rotate K at positions j
-    for (int e = threadIdx.x; e < kTileK * D; e += blockDim.x) {
-      const int jj = e / D, d = e - jj * D;
-      sK[e] = jj < nk ? rotated(sRaw + jj * D, d, j0 + jj, p) : 0.f;
+    // rotate K at positions j, pair by pair
+    for (int e = threadIdx.x; e < kTileK * half; e += blockDim.x) {
+      const int jj = e / half, pi = e - jj * half;
+      if (jj < nk) rotate_pair(sK + jj * DP, pi, j0 + jj, p);
     }
     __syncthreads();
 
     if (row_ok) {
-      float my_s = -INFINITY;
-      for (int jj = 0; jj < kTileK; ++jj) {
-        float part = 0.f;
-#pragma unroll
-        for (int u = 0; u < kMaxPerLane; ++u) {
-          const int d = lane + 32 * u;
-          if (d < D) part += qr[u] * sK[jj * D + d];
-        }
-        part = warp_sum(part);
-        const int64_t j = j0 + jj;
-        if (lane == jj && jj < nk && j <= qpos) my_s = part * p.scale;
+      // lane jj scores key j0 + jj (four partial sums to shorten the chain)
+      const float *kr = sK + lane * DP;
+      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+      int d = 0;
+      for (; d + 4 <= D; d += 4) {
+        s0 = fmaf(qs[d], kr[d], s0);
+        s1 = fmaf(qs[d + 1], kr[d + 1], s1);
+        s2 = fmaf(qs[d + 2], kr[d + 2], s2);
+        s3 = fmaf(qs[d + 3], kr[d + 3], s3);
       }
+      for (; d < D; ++d) s0 = fmaf(qs[d], kr[d], s0);
+      const int64_t j = j0 + lane;
+      const float my_s = (lane < nk && j <= qpos) ? ((s0 + s1) + (s2 + s3)) * p.scale : -INFINITY;
       const float tmax = warp_max(my_s);
       if (tmax != -INFINITY) {
         const float m_new = fmaxf(m, tmax);
@@ -188,7 +181,7 @@ cudaError_t launch_attn_simt(const AttnArgs &a, cudaStream_t s) {
   for (int j = 0; j < 3; ++j) {
     p.sq[j] = a.sq[j]; p.sk[j] = a.sk[j]; p.sv[j] = a.sv[j]; p.so[j] = a.so[j];
   }
-  const size_t smem = (size_t)3 * kTileK * a.D * sizeof(float);
+  const size_t smem = ((size_t)kTileK * (a.D + 1) + (size_t)kTileK * a.D + (size_t)kRows * a.D) * sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(attn_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
