@@ -233,3 +233,32 @@ def test_unfused_rotate_then_flash_matches(ra, orc, layout):
     o_ref, _ = orc.attention(q.float().numpy(), k.float().numpy(), v.float().numpy(),
                              layout=layout)
     assert np.abs(o_u.float().cpu().numpy() - o_ref).max() <= 2e-2
+
+
+def test_past_2g_elements_sampled_rows(ra, orc):
+    """Q, K, V and O with more than 2^31 elements each (1040 x 16 x 1024 x 128,
+    4.4 GB per tensor): 64-bit offsets in every tensor map and store.  One
+    seeded batch is repeated along B on the device, so every batch computes
+    the same attention; 256 sampled rows and the edge rows of the first and
+    the last batch are checked against the oracle on that batch."""
+    B, H, S, D = 1040, 16, 1024, 128
+    qb, kb, vb = wl.attn_qkv(1, H, H, S, S, D, torch.bfloat16, 41)
+    qg, kg, vg = [t.cuda().expand(B, H, S, D).contiguous() for t in (qb, kb, vb)]
+    assert qg.numel() > 2 ** 31
+    cos, sin = ra.make_tables(S, D, 10000.0)
+    o, lse = ra.attn_fwd_causal_rope(qg, kg, vg, cos, sin)
+    assert ra.ra_get_device_status() == 0
+    del qg, kg, vg
+    rng = np.random.default_rng(42)
+    rows = np.unique(np.concatenate([rng.integers(0, H * S, 256), np.arange(128),
+                                     np.arange(H * S - 128, H * S)]))
+    o_ref, lse_ref = orc.attention(qb.float().numpy(), kb.float().numpy(), vb.float().numpy(),
+                                   rows=rows)
+    to, tl = TOL[torch.bfloat16]
+    for bi in (0, B - 1):
+        og = o[bi].reshape(-1, D)[torch.from_numpy(rows).cuda()].float().cpu().numpy()
+        lg = lse[bi].reshape(-1)[torch.from_numpy(rows).cuda()].cpu().numpy()
+        assert np.abs(og - o_ref).max() <= to
+        assert np.abs(lg - lse_ref).max() <= tl
+    del o, lse
+    torch.cuda.empty_cache()

@@ -218,3 +218,29 @@ def test_interpolated_tables_match_oracle(ra, orc, scale, rows, rot_dim, base):
         want_q[t, :, :half] = lo * wc[pos[t]] - hi * ws[pos[t]]
         want_q[t, :, half:] = hi * wc[pos[t]] + lo * ws[pos[t]]
     assert np.abs(qg.cpu().double().numpy() - want_q).max() <= 1e-5
+
+
+def test_past_2g_elements_sampled_tokens(ra, orc):
+    """Q with more than 2^31 elements (2^21 + 7 tokens x 8 heads x 128, 4.3 GB):
+    64-bit token offsets.  A seeded 4096-token block is repeated along T on
+    the device and every token takes a random position; tokens at both ends
+    and 512 sampled tokens are checked against the oracle."""
+    T, Hq, Hkv, D, R = (1 << 21) + 7, 8, 2, 128, 32768
+    qb, kb, _ = wl.attn_qkv(1, Hq, Hkv, 4096, 4096, D, torch.bfloat16, 31)
+    qb, kb = qb[0].transpose(0, 1).contiguous(), kb[0].transpose(0, 1).contiguous()  # [4096, H, D]
+    reps = (T + 4095) // 4096
+    qg = qb.cuda().repeat(reps, 1, 1)[:T].contiguous()
+    kg = kb.cuda().repeat(reps, 1, 1)[:T].contiguous()
+    assert qg.numel() > 2 ** 31
+    pos = np.random.default_rng(31).integers(0, R, T).astype(np.int32)
+    cos, sin = ra.make_tables(R, D, 10000.0)
+    ra.rope_apply_qk(qg, kg, torch.from_numpy(pos).cuda(), cos, sin, layout=NEOX)
+    assert ra.ra_get_device_status() == 0
+    rng = np.random.default_rng(32)
+    sel = np.unique(np.concatenate([np.arange(16), np.arange(T - 16, T), rng.integers(0, T, 512)]))
+    idx = torch.from_numpy(sel)
+    src = torch.from_numpy(sel % 4096)
+    check_rotated(qg[idx.cuda()].cpu(), qb[src], pos[sel], orc, D, 10000.0, NEOX)
+    check_rotated(kg[idx.cuda()].cpu(), kb[src], pos[sel], orc, D, 10000.0, NEOX)
+    del qg, kg
+    torch.cuda.empty_cache()
