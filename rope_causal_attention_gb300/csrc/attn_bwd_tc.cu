@@ -50,7 +50,6 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
-#include <mutex>
 #include <type_traits>
 
 #include "common.cuh"
@@ -800,14 +799,14 @@ cudaError_t rotate_f16(const void *x, int B, int H, int64_t S, int D, const int6
 template <int D, typename TIn>
 cudaError_t launch_typed(const CUtensorMap (&maps)[4], const BwdTcParams &p, cudaStream_t s) {
   using C = BCfg<D>;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(bwd_dkdv_tc_kernel<D, TIn>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, C::K_SMEM);
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(bwd_dq_tc_kernel<D, TIn>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, C::Q_SMEM);
+  static PerDeviceOnce once;
+  const cudaError_t attr_err = once.run([] {
+    cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_tc_kernel<D, TIn>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::K_SMEM);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(bwd_dq_tc_kernel<D, TIn>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::Q_SMEM);
+    return e;
   });
   if (attr_err != cudaSuccess) return attr_err;
   const int64_t gk = (int64_t)p.n_kt * p.B * p.Hkv;

@@ -42,7 +42,6 @@
 #include <math.h>
 #include <stdlib.h>
 
-#include <mutex>
 #include <type_traits>
 
 #include "common.cuh"
@@ -1032,16 +1031,16 @@ template <int D, typename TIn>
 cudaError_t launch_typed(const AttnArgs &a, const CUtensorMap &kmap, const CUtensorMap &vmap,
                          const TcParams &p, unsigned grid, cudaStream_t s) {
   using C = TcCfg<D>;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(attn_tc_kernel<D, TIn>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  static PerDeviceOnce once;
+  const cudaError_t attr_err = once.run([] {
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, TIn>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     // The setmaxnreg shares add up to 512 threads x 128 registers: a build
     // that allocated anything else could leave an increase waiting forever.
     cudaFuncAttributes fa;
-    if (attr_err == cudaSuccess) attr_err = cudaFuncGetAttributes(&fa, attn_tc_kernel<D, TIn>);
-    if (attr_err == cudaSuccess && fa.numRegs != 128) attr_err = cudaErrorInvalidConfiguration;
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, attn_tc_kernel<D, TIn>);
+    if (e == cudaSuccess && fa.numRegs != 128) e = cudaErrorInvalidConfiguration;
+    return e;
   });
   if (attr_err != cudaSuccess) return attr_err;
   attn_tc_kernel<D, TIn><<<grid, kThreads, C::SMEM, s>>>(kmap, vmap, p);

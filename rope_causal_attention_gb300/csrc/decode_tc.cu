@@ -31,7 +31,6 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
-#include <mutex>
 #include <type_traits>
 
 #include "common.cuh"
@@ -452,11 +451,10 @@ template <typename TIn, int NPAD>
 cudaError_t launch_typed(const CUtensorMap &mk, const CUtensorMap &mv, const DTcParams &p,
                          const DecodeArgs &a, cudaStream_t s) {
   using C = DCfg<NPAD>;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(attn_decode_tc_kernel<TIn, NPAD>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  static PerDeviceOnce once;
+  const cudaError_t attr_err = once.run([] {
+    return cudaFuncSetAttribute(attn_decode_tc_kernel<TIn, NPAD>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   });
   if (attr_err != cudaSuccess) return attr_err;
   if (a.plan.chunk > (int64_t)C::TILES * 128) return cudaErrorInvalidValue;  // plan mismatch

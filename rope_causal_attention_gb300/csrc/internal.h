@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/rope_attn.h"
 
 namespace ra {
@@ -137,6 +139,32 @@ cudaError_t launch_attn_decode(const DecodeArgs &a, cudaStream_t s);
 // has no variant for the case.
 cudaError_t launch_attn_decode_tc(const DecodeArgs &a, cudaStream_t s);
 int sm_count_current();
+
+// One-time set-up (kernel attributes) per device: a function attribute
+// belongs to the device that was current when it was set, so a process that
+// drives several GPUs sets it on each.  run() returns the set-up's result.
+class PerDeviceOnce {
+ public:
+  template <typename F>
+  cudaError_t run(F &&f) {
+    int dev = 0;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return f();
+    std::lock_guard<std::mutex> lock(mutex_);
+    if (!done_[dev]) {
+      result_[dev] = f();
+      done_[dev] = true;
+    }
+    return result_[dev];
+  }
+
+ private:
+  static constexpr int kMaxDevices = 64;
+  std::mutex mutex_;
+  bool done_[kMaxDevices] = {};
+  cudaError_t result_[kMaxDevices] = {};
+};
 
 // A 16-bit tensor (bf16 or fp16) whose rows of D elements are contiguous,
 // addressed by n_outer (1..3) further coordinates with the given sizes and
