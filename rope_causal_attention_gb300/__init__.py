@@ -45,12 +45,16 @@ class KVCacheDesc(ctypes.Structure):
 
 
 class RAError(RuntimeError):
+    """A non-OK ra_status from the library: `code` is the status value, the
+    message carries ra_status_string and the library's reason (ra_last_error)."""
+
     def __init__(self, code: int, msg: str):
         super().__init__(msg)
         self.code = code
 
 
 def library_path() -> str:
+    """Path of the shared library the binding loads (built in-tree by build())."""
     return _LIB_PATH
 
 
@@ -110,6 +114,7 @@ def lib():
 
 
 def ra_status_string(code: int) -> str:
+    """English name of an ra_status code."""
     return lib().ra_status_string(int(code)).decode()
 
 
