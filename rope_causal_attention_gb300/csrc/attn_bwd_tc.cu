@@ -155,6 +155,11 @@ __device__ __forceinline__ void wait_bar_drain(uint32_t bar, uint32_t parity) {
     if (clock64() - t0 > kTimeoutCycles) return;
 }
 
+// Bounded wait taken by a whole warp (the MMA issuers run warp-wide).
+__device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, const Ctl &c) {
+  return __all_sync(0xffffffffu, wait_bar(bar, parity, c));
+}
+
 __device__ __forceinline__ int map_coord(const int perm, int row, int head, int b) {
   return perm == 0 ? row : (perm == 1 ? head : b);
 }
@@ -444,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int u = max(0, issued - C::NS); u < issued; ++u)
           wait_bar_drain(bar(C::KB_QFULL + u % C::NS), (uint32_t)((u / C::NS) & 1));
     }
-  } else if (lane == 0) {
+  } else {  // MMA issuer: the whole warp, one elected lane issues
     // =================================================================== MMA
     constexpr uint32_t ab = std::is_same<TIn, __nv_bfloat16>::value ? 1u : 0u;
     constexpr uint32_t IDESC_S = idesc_f16(0u, 0u, 128);   // fp16 K~ x Q~^T
@@ -458,10 +463,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t do_lo0 = sdesc_lo(sbase + C::K_OFF_DO, 16);
     const uint32_t qmn_lo0 = sdesc_lo(sbase + C::K_OFF_Q, C::SUBT);
     const uint32_t domn_lo0 = sdesc_lo(sbase + C::K_OFF_DO, C::SUBT);
-    bool ok = NU == 0 || wait_bar(bar(C::KB_KVFULL), 0u, ctl);
+    bool ok = NU == 0 || wait_all(bar(C::KB_KVFULL), 0u, ctl);
     for (int u = 0; ok && u < NU; ++u) {
       const int st = u % C::NS;
-      if (!wait_bar(bar(C::KB_QFULL + st), (uint32_t)((u / C::NS) & 1), ctl)) {
+      if (!wait_all(bar(C::KB_QFULL + st), (uint32_t)((u / C::NS) & 1), ctl)) {
         ok = false;
         break;
       }
@@ -470,18 +475,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (uint32_t)(((kk >> 2) * C::SUBT + (kk & 3) * 32) >> 4);
-        mma_ss(tmem + 256u, sdesc_join(k_lo + off, HI), sdesc_join(q_lo0 + so + off, HI),
+        mma_ss_w(tmem + 256u, sdesc_join(k_lo + off, HI), sdesc_join(q_lo0 + so + off, HI),
                IDESC_S, kk > 0 ? 1u : 0u);
       }
-      tc_commit(bar(C::KB_SFULL));
+      tc_commit_w(bar(C::KB_SFULL));
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (uint32_t)(((kk >> 2) * C::SUBT + (kk & 3) * 32) >> 4);
-        mma_ss(tmem + 384u, sdesc_join(v_lo + off, HI), sdesc_join(do_lo0 + so + off, HI),
+        mma_ss_w(tmem + 384u, sdesc_join(v_lo + off, HI), sdesc_join(do_lo0 + so + off, HI),
                IDESC_DP, kk > 0 ? 1u : 0u);
       }
-      tc_commit(bar(C::KB_DPFULL));
-      if (!wait_bar(bar(C::KB_PFULL), (uint32_t)(u & 1), ctl)) {
+      tc_commit_w(bar(C::KB_DPFULL));
+      if (!wait_all(bar(C::KB_PFULL), (uint32_t)(u & 1), ctl)) {
         ok = false;
         break;
       }
@@ -489,18 +494,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       // 16 queries per step; queries 64..127 were packed at column +64
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_ts(tmem, tmem + 256u + (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8),
+        mma_ts_w(tmem, tmem + 256u + (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8),
                sdesc_join(domn_lo0 + so + (uint32_t)(kk * 2048 >> 4), HI), IDESC_DV,
                (u > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_ts(tmem + (uint32_t)D, tmem + 384u + (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8),
+        mma_ts_w(tmem + (uint32_t)D, tmem + 384u + (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8),
                sdesc_join(qmn_lo0 + so + (uint32_t)(kk * 2048 >> 4), HI), IDESC_DK,
                (u > 0 || kk > 0) ? 1u : 0u);
-      tc_commit(bar(C::KB_QEMPTY + st));
+      tc_commit_w(bar(C::KB_QEMPTY + st));
     }
-    if (ok && NU > 0) tc_commit(bar(C::KB_ACC));
-    tc_commit(bar(C::KB_DONE));
+    if (ok && NU > 0) tc_commit_w(bar(C::KB_ACC));
+    tc_commit_w(bar(C::KB_DONE));
     wait_bar_drain(bar(C::KB_DONE), 0u);
   }
 
@@ -690,7 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           wait_bar_drain(bar(C::QB_VFULL + n % C::NSV), (uint32_t)((n / C::NSV) & 1));
       }
     }
-  } else if (lane == 0) {
+  } else {  // MMA issuer: the whole warp, one elected lane issues
     // =================================================================== MMA
     constexpr uint32_t ab = std::is_same<TIn, __nv_bfloat16>::value ? 1u : 0u;
     constexpr uint32_t IDESC_S = idesc_f16(0u, 0u, 128);   // fp16 Q~ x K~^T
@@ -702,23 +707,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t k_lo0 = sdesc_lo(sbase + C::Q_OFF_K, 16);
     const uint32_t v_lo0 = sdesc_lo(sbase + C::Q_OFF_V, 16);
     const uint32_t kmn_lo0 = sdesc_lo(sbase + C::Q_OFF_K, C::SUBT);
-    bool ok = wait_bar(bar(C::QB_QFULL), 0u, ctl);
+    bool ok = wait_all(bar(C::QB_QFULL), 0u, ctl);
     // dQ~ += dS(m) K~(m), A = dS packed in S slot m & 1 (keys 64..127 at +64)
     auto issue_dq = [&](int mm) {
       const int st = mm % C::NSK, sl = mm & 1;
       const uint32_t so = (uint32_t)(st * C::TILE >> 4);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_ts(tmem + 384u, tmem + (uint32_t)(128 * sl + (kk >> 2) * 64 + (kk & 3) * 8),
+        mma_ts_w(tmem + 384u, tmem + (uint32_t)(128 * sl + (kk >> 2) * 64 + (kk & 3) * 8),
                sdesc_join(kmn_lo0 + so + (uint32_t)(kk * 2048 >> 4), HI), IDESC_DQ,
                (mm > 0 || kk > 0) ? 1u : 0u);
-      tc_commit(bar(C::QB_KEMPTY + st));
+      tc_commit_w(bar(C::QB_KEMPTY + st));
     };
     // Issue order S(n), dP(n), dQ~(n-1): the tensor core computes the next
     // tile's S and dP while the threads turn this tile's into dS.
     for (int n = 0; ok && n < N; ++n) {
       const int stk = n % C::NSK, stv = n % C::NSV, sl = n & 1;
-      if (!wait_bar(bar(C::QB_KFULL + stk), (uint32_t)((n / C::NSK) & 1), ctl)) {
+      if (!wait_all(bar(C::QB_KFULL + stk), (uint32_t)((n / C::NSK) & 1), ctl)) {
         ok = false;
         break;
       }
@@ -727,12 +732,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (uint32_t)(((kk >> 2) * C::SUBT + (kk & 3) * 32) >> 4);
-        mma_ss(tmem + (uint32_t)(128 * sl), sdesc_join(q_lo + off, HI),
+        mma_ss_w(tmem + (uint32_t)(128 * sl), sdesc_join(q_lo + off, HI),
                sdesc_join(k_lo0 + sok + off, HI), IDESC_S, kk > 0 ? 1u : 0u);
       }
-      tc_commit(bar(C::QB_SFULL + sl));
-      if (!wait_bar(bar(C::QB_VFULL + stv), (uint32_t)((n / C::NSV) & 1), ctl) ||
-          (n >= 1 && !wait_bar(bar(C::QB_DPFREE), (uint32_t)((n - 1) & 1), ctl))) {
+      tc_commit_w(bar(C::QB_SFULL + sl));
+      if (!wait_all(bar(C::QB_VFULL + stv), (uint32_t)((n / C::NSV) & 1), ctl) ||
+          (n >= 1 && !wait_all(bar(C::QB_DPFREE), (uint32_t)((n - 1) & 1), ctl))) {
         ok = false;
         break;
       }
@@ -740,13 +745,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (uint32_t)(((kk >> 2) * C::SUBT + (kk & 3) * 32) >> 4);
-        mma_ss(tmem + 256u, sdesc_join(do_lo + off, HI), sdesc_join(v_lo0 + sov + off, HI),
+        mma_ss_w(tmem + 256u, sdesc_join(do_lo + off, HI), sdesc_join(v_lo0 + sov + off, HI),
                IDESC_DP, kk > 0 ? 1u : 0u);
       }
-      tc_commit(bar(C::QB_DPFULL));
-      tc_commit(bar(C::QB_VEMPTY + stv));
+      tc_commit_w(bar(C::QB_DPFULL));
+      tc_commit_w(bar(C::QB_VEMPTY + stv));
       if (n >= 1) {
-        if (!wait_bar(bar(C::QB_PFULL + ((n - 1) & 1)), (uint32_t)(((n - 1) >> 1) & 1), ctl)) {
+        if (!wait_all(bar(C::QB_PFULL + ((n - 1) & 1)), (uint32_t)(((n - 1) >> 1) & 1), ctl)) {
           ok = false;
           break;
         }
@@ -755,14 +760,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (ok && N > 0) {
-      ok = wait_bar(bar(C::QB_PFULL + ((N - 1) & 1)), (uint32_t)(((N - 1) >> 1) & 1), ctl);
+      ok = wait_all(bar(C::QB_PFULL + ((N - 1) & 1)), (uint32_t)(((N - 1) >> 1) & 1), ctl);
       if (ok) {
         tc_fence_after();
         issue_dq(N - 1);
-        tc_commit(bar(C::QB_ACC));
+        tc_commit_w(bar(C::QB_ACC));
       }
     }
-    tc_commit(bar(C::QB_DONE));
+    tc_commit_w(bar(C::QB_DONE));
     wait_bar_drain(bar(C::QB_DONE), 0u);
   }
 

@@ -144,6 +144,11 @@ __device__ __forceinline__ void wait_bar_drain(uint32_t bar, uint32_t parity) {
     if (clock64() - t0 > kTimeoutCycles) return;
 }
 
+// Bounded wait taken by a whole warp (the MMA issuers run warp-wide).
+__device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, const Ctl &c) {
+  return __all_sync(0xffffffffu, wait_bar(bar, parity, c));
+}
+
 template <typename T> struct In16;
 template <> struct In16<__nv_bfloat16> {
   static __device__ __forceinline__ void unpack(const uint4 &u, float *f) {
@@ -898,117 +903,117 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (warp == kWarpMma) {
       // ================================================================== MMA
-      if (lane == 0) {
-        constexpr uint32_t tin_bf16 = std::is_same<TIn, __nv_bfloat16>::value ? 1u : 0u;
-        constexpr uint32_t IDESC_S = idesc_f16(0u, 0u, 128);      // fp16 x fp16, K-major B
-        constexpr uint32_t IDESC_PV = idesc_f16(tin_bf16, 1u, D);  // P x V, V N-major
-        // descriptor low words of every tile base, computed once; each K=16
-        // step then adds a constant ((offset >> 4) of the step)
-        constexpr uint32_t HI = sdesc_hi_sw128(1024);
-        const uint32_t q_lo0 = sdesc_lo(sbase + C::OFF_Q, 16);
-        const uint32_t k_lo0 = sdesc_lo(sbase + C::OFF_K, 16);
-        const uint32_t v_lo0 = sdesc_lo(sbase + C::OFF_V, C::SUBT);
-        auto mma_s = [&](int s, int st) {
-          const uint32_t qlo = q_lo0 + (uint32_t)((p.split ? 0 : s) * C::TILE >> 4);
-          const uint32_t klo = k_lo0 + (uint32_t)(st * C::TILE >> 4);
-          const uint32_t dS = tmem + C::s_col(s);
+      // whole warp; one elected lane issues
+      constexpr uint32_t tin_bf16 = std::is_same<TIn, __nv_bfloat16>::value ? 1u : 0u;
+      constexpr uint32_t IDESC_S = idesc_f16(0u, 0u, 128);      // fp16 x fp16, K-major B
+      constexpr uint32_t IDESC_PV = idesc_f16(tin_bf16, 1u, D);  // P x V, V N-major
+      // descriptor low words of every tile base, computed once; each K=16
+      // step then adds a constant ((offset >> 4) of the step)
+      constexpr uint32_t HI = sdesc_hi_sw128(1024);
+      const uint32_t q_lo0 = sdesc_lo(sbase + C::OFF_Q, 16);
+      const uint32_t k_lo0 = sdesc_lo(sbase + C::OFF_K, 16);
+      const uint32_t v_lo0 = sdesc_lo(sbase + C::OFF_V, C::SUBT);
+      auto mma_s = [&](int s, int st) {
+        const uint32_t qlo = q_lo0 + (uint32_t)((p.split ? 0 : s) * C::TILE >> 4);
+        const uint32_t klo = k_lo0 + (uint32_t)(st * C::TILE >> 4);
+        const uint32_t dS = tmem + C::s_col(s);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = ((kk >> 2) * C::SUBT + (kk & 3) * 32) >> 4;
-            mma_ss(dS, sdesc_join(qlo + off, HI), sdesc_join(klo + off, HI), IDESC_S,
-                   kk > 0 ? 1u : 0u);
-          }
-        };
-        auto mma_pv = [&](int s, int st, bool acc) {
-          const uint32_t vlo = v_lo0 + (uint32_t)(st * C::TILE >> 4);
-          const uint32_t dO = tmem + C::o_col(s), aP = tmem + C::s_col(s);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * C::SUBT + (kk & 3) * 32) >> 4;
+          mma_ss_w(dS, sdesc_join(qlo + off, HI), sdesc_join(klo + off, HI), IDESC_S,
+                 kk > 0 ? 1u : 0u);
+        }
+      };
+      auto mma_pv = [&](int s, int st, bool acc) {
+        const uint32_t vlo = v_lo0 + (uint32_t)(st * C::TILE >> 4);
+        const uint32_t dO = tmem + C::o_col(s), aP = tmem + C::s_col(s);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ts(dO, aP + kk * 8, sdesc_join(vlo + (uint32_t)(kk * 2048 >> 4), HI), IDESC_PV,
-                   (acc || kk > 0) ? 1u : 0u);
-        };
-        auto part = [&](int s, int n) { return n < (s ? nend1 : nend0); };
-        bool ok = true;
-        if (p.split) {
-          // both slots read query buffer 0; each K/V stream entry has one user
-          ok = wait_bar(bar(C::B_QFULL + 0), 0u, ctl);
-          for (int s = 0; ok && s < 2; ++s) {
-            if (!part(s, 0)) continue;
-            const int e = split_entry(s, 0, nend1), st = e % C::NS;
-            if (!wait_bar(bar(C::B_KFULL + st), (uint32_t)((e / C::NS) & 1), ctl)) { ok = false; break; }
-            mma_s(s, st);
-            tc_commit(bar(C::B_SFULL + s));
-            tc_commit(bar(C::B_KEMPTY + st));
-          }
-          for (int n = 0; ok && n < nend0; ++n) {
-            for (int s = 0; s < 2; ++s) {
-              if (!part(s, n)) continue;
-              const int e = split_entry(s, n, nend1), st = e % C::NS;
-              if (!wait_bar(bar(C::B_VFULL + st), (uint32_t)((e / C::NS) & 1), ctl) ||
-                  !wait_bar(bar(C::B_PFULL + s), (uint32_t)(n & 1), ctl)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              mma_pv(s, st, n > 0);
-              tc_commit(bar(C::B_VEMPTY + st));
-              if (!part(s, n + 1)) {
-                tc_commit(bar(C::B_OFULL + s));
-                continue;
-              }
-              const int e2 = split_entry(s, n + 1, nend1), st2 = e2 % C::NS;
-              if (!wait_bar(bar(C::B_KFULL + st2), (uint32_t)((e2 / C::NS) & 1), ctl)) {
-                ok = false;
-                break;
-              }
-              mma_s(s, st2);
-              tc_commit(bar(C::B_SFULL + s));
-              tc_commit(bar(C::B_KEMPTY + st2));
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts_w(dO, aP + kk * 8, sdesc_join(vlo + (uint32_t)(kk * 2048 >> 4), HI), IDESC_PV,
+                 (acc || kk > 0) ? 1u : 0u);
+      };
+      auto part = [&](int s, int n) { return n < (s ? nend1 : nend0); };
+      bool ok = true;
+      if (p.split) {
+        // both slots read query buffer 0; each K/V stream entry has one user
+        ok = wait_all(bar(C::B_QFULL + 0), 0u, ctl);
+        for (int s = 0; ok && s < 2; ++s) {
+          if (!part(s, 0)) continue;
+          const int e = split_entry(s, 0, nend1), st = e % C::NS;
+          if (!wait_all(bar(C::B_KFULL + st), (uint32_t)((e / C::NS) & 1), ctl)) { ok = false; break; }
+          mma_s(s, st);
+          tc_commit_w(bar(C::B_SFULL + s));
+          tc_commit_w(bar(C::B_KEMPTY + st));
+        }
+        for (int n = 0; ok && n < nend0; ++n) {
+          for (int s = 0; s < 2; ++s) {
+            if (!part(s, n)) continue;
+            const int e = split_entry(s, n, nend1), st = e % C::NS;
+            if (!wait_all(bar(C::B_VFULL + st), (uint32_t)((e / C::NS) & 1), ctl) ||
+                !wait_all(bar(C::B_PFULL + s), (uint32_t)(n & 1), ctl)) {
+              ok = false;
+              break;
             }
-          }
-        } else {
-          if (act0) ok = wait_bar(bar(C::B_QFULL + 0), 0u, ctl);
-          if (ok && act1) ok = wait_bar(bar(C::B_QFULL + 1), 0u, ctl);
-          if (ok && N > 0) ok = wait_bar(bar(C::B_KFULL + 0), 0u, ctl);
-          if (ok && N > 0) {
-            for (int s = 0; s < 2; ++s)
-              if (part(s, 0)) {
-                mma_s(s, 0);
-                tc_commit(bar(C::B_SFULL + s));
-              }
-            tc_commit(bar(C::B_KEMPTY + 0));
-          }
-          for (int n = 0; ok && n < N; ++n) {
-            const int st = n % C::NS, nst = (n + 1) % C::NS;
-            if (!wait_bar(bar(C::B_VFULL + st), (uint32_t)((n / C::NS) & 1), ctl)) { ok = false; break; }
-            bool k_next = false;
-            for (int s = 0; s < 2; ++s) {
-              if (!part(s, n)) continue;
-              if (!wait_bar(bar(C::B_PFULL + s), (uint32_t)(n & 1), ctl)) { ok = false; break; }
-              tc_fence_after();
-              mma_pv(s, st, n > 0);
-              if (n == (s ? nend1 : nend0) - 1) tc_commit(bar(C::B_OFULL + s));
-              if (part(s, n + 1)) {
-                if (!k_next) {
-                  if (!wait_bar(bar(C::B_KFULL + nst), (uint32_t)(((n + 1) / C::NS) & 1), ctl)) {
-                    ok = false;
-                    break;
-                  }
-                  k_next = true;
-                }
-                mma_s(s, nst);
-                tc_commit(bar(C::B_SFULL + s));
-              }
+            tc_fence_after();
+            mma_pv(s, st, n > 0);
+            tc_commit_w(bar(C::B_VEMPTY + st));
+            if (!part(s, n + 1)) {
+              tc_commit_w(bar(C::B_OFULL + s));
+              continue;
             }
-            if (!ok) break;
-            tc_commit(bar(C::B_VEMPTY + st));
-            if (k_next) tc_commit(bar(C::B_KEMPTY + nst));
+            const int e2 = split_entry(s, n + 1, nend1), st2 = e2 % C::NS;
+            if (!wait_all(bar(C::B_KFULL + st2), (uint32_t)((e2 / C::NS) & 1), ctl)) {
+              ok = false;
+              break;
+            }
+            mma_s(s, st2);
+            tc_commit_w(bar(C::B_SFULL + s));
+            tc_commit_w(bar(C::B_KEMPTY + st2));
           }
         }
-        // all issued MMAs complete before tensor memory is released
-        tc_commit(bar(C::B_DONE));
-        wait_bar_drain(bar(C::B_DONE), 0u);
+      } else {
+        if (act0) ok = wait_all(bar(C::B_QFULL + 0), 0u, ctl);
+        if (ok && act1) ok = wait_all(bar(C::B_QFULL + 1), 0u, ctl);
+        if (ok && N > 0) ok = wait_all(bar(C::B_KFULL + 0), 0u, ctl);
+        if (ok && N > 0) {
+          for (int s = 0; s < 2; ++s)
+            if (part(s, 0)) {
+              mma_s(s, 0);
+              tc_commit_w(bar(C::B_SFULL + s));
+            }
+          tc_commit_w(bar(C::B_KEMPTY + 0));
+        }
+        for (int n = 0; ok && n < N; ++n) {
+          const int st = n % C::NS, nst = (n + 1) % C::NS;
+          if (!wait_all(bar(C::B_VFULL + st), (uint32_t)((n / C::NS) & 1), ctl)) { ok = false; break; }
+          bool k_next = false;
+          for (int s = 0; s < 2; ++s) {
+            if (!part(s, n)) continue;
+            if (!wait_all(bar(C::B_PFULL + s), (uint32_t)(n & 1), ctl)) { ok = false; break; }
+            tc_fence_after();
+            mma_pv(s, st, n > 0);
+            if (n == (s ? nend1 : nend0) - 1) tc_commit_w(bar(C::B_OFULL + s));
+            if (part(s, n + 1)) {
+              if (!k_next) {
+                if (!wait_all(bar(C::B_KFULL + nst), (uint32_t)(((n + 1) / C::NS) & 1), ctl)) {
+                  ok = false;
+                  break;
+                }
+                k_next = true;
+              }
+              mma_s(s, nst);
+              tc_commit_w(bar(C::B_SFULL + s));
+            }
+          }
+          if (!ok) break;
+          tc_commit_w(bar(C::B_VEMPTY + st));
+          if (k_next) tc_commit_w(bar(C::B_KEMPTY + nst));
+        }
       }
+      // all issued MMAs complete before tensor memory is released
+      tc_commit_w(bar(C::B_DONE));
+      wait_bar_drain(bar(C::B_DONE), 0u);
+
     }
   }
 

@@ -112,6 +112,11 @@ __device__ __forceinline__ void wait_bar_drain(uint32_t bar, uint32_t parity) {
     if (clock64() - t0 > kTimeoutCycles) return;
 }
 
+// Bounded wait taken by a whole warp (the MMA issuers run warp-wide).
+__device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, const Ctl &c) {
+  return __all_sync(0xffffffffu, wait_bar(bar, parity, c));
+}
+
 __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
@@ -224,60 +229,60 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   } else if (warp == kWarpMma) {
     // ================================================================ MMA
-    if (lane == 0) {
-      constexpr uint32_t ab = std::is_same<TIn, __nv_bfloat16>::value ? 1u : 0u;
-      constexpr uint32_t IDESC_S = idesc_f16_ab(ab, 0u, 0u, NPAD);  // K x Q^T
-      constexpr uint32_t IDESC_O = idesc_f16_ab(ab, 1u, 0u, NPAD);  // V^T (MN-major) x P^T
-      constexpr uint32_t HI = sdesc_hi_sw128(1024);
-      const uint32_t k_lo0 = sdesc_lo(sbase + C::OFF_KV, 16);
-      const uint32_t v_lo0 = sdesc_lo(sbase + C::OFF_KV, kHalfBytes);
-      const uint32_t q_lo0 = sdesc_lo(sbase + C::OFF_Q, 16);
-      const uint32_t p_lo0 = sdesc_lo(sbase + C::OFF_P, 16);
-      bool ok = wait_bar(bar(C::B_QFULL), 0u, ctl);
-      for (int t = 0; ok && t < T; ++t) {
-        const int st = t % C::NS;
-        if (!wait_bar(bar(C::B_FULL + st), (uint32_t)((t / C::NS) & 1), ctl)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t a_lo = k_lo0 + (uint32_t)(st * kTileBytes >> 4);
-        const uint32_t dS = tmem + (uint32_t)(NPAD * (1 + t));
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t oa = (uint32_t)(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
-          const uint32_t ob = (uint32_t)(((kk >> 2) * (NPAD * 128) + (kk & 3) * 32) >> 4);
-          mma_ss(dS, sdesc_join(a_lo + oa, HI), sdesc_join(q_lo0 + ob, HI), IDESC_S,
-                 kk > 0 ? 1u : 0u);
-        }
-        tc_commit(bar(C::B_EMPTY + st));
+    // whole warp; one elected lane issues
+    constexpr uint32_t ab = std::is_same<TIn, __nv_bfloat16>::value ? 1u : 0u;
+    constexpr uint32_t IDESC_S = idesc_f16_ab(ab, 0u, 0u, NPAD);  // K x Q^T
+    constexpr uint32_t IDESC_O = idesc_f16_ab(ab, 1u, 0u, NPAD);  // V^T (MN-major) x P^T
+    constexpr uint32_t HI = sdesc_hi_sw128(1024);
+    const uint32_t k_lo0 = sdesc_lo(sbase + C::OFF_KV, 16);
+    const uint32_t v_lo0 = sdesc_lo(sbase + C::OFF_KV, kHalfBytes);
+    const uint32_t q_lo0 = sdesc_lo(sbase + C::OFF_Q, 16);
+    const uint32_t p_lo0 = sdesc_lo(sbase + C::OFF_P, 16);
+    bool ok = wait_all(bar(C::B_QFULL), 0u, ctl);
+    for (int t = 0; ok && t < T; ++t) {
+      const int st = t % C::NS;
+      if (!wait_all(bar(C::B_FULL + st), (uint32_t)((t / C::NS) & 1), ctl)) {
+        ok = false;
+        break;
       }
-      if (ok) tc_commit(bar(C::B_SFULL));
-      for (int t = 0; ok && t < T; ++t) {
-        const int n = T + t, st = n % C::NS;
-        if (!wait_bar(bar(C::B_FULL + st), (uint32_t)((n / C::NS) & 1), ctl) ||
-            !wait_bar(bar(C::B_PFULL + (t & 1)), (uint32_t)((t >> 1) & 1), ctl)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t a_lo = v_lo0 + (uint32_t)(st * kTileBytes >> 4);
-        const uint32_t b_lo = p_lo0 + (uint32_t)((t & 1) * C::PB >> 4);
+      tc_fence_after();
+      const uint32_t a_lo = k_lo0 + (uint32_t)(st * kTileBytes >> 4);
+      const uint32_t dS = tmem + (uint32_t)(NPAD * (1 + t));
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t oa = (uint32_t)((kk * 2048) >> 4);  // 16 keys x 128 bytes
-          const uint32_t ob = (uint32_t)(((kk >> 2) * (NPAD * 128) + (kk & 3) * 32) >> 4);
-          mma_ss(tmem, sdesc_join(a_lo + oa, HI), sdesc_join(b_lo + ob, HI), IDESC_O,
-                 (t > 0 || kk > 0) ? 1u : 0u);
-        }
-        tc_commit(bar(C::B_EMPTY + st));
-        tc_commit(bar(C::B_PEMPTY + (t & 1)));
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t oa = (uint32_t)(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
+        const uint32_t ob = (uint32_t)(((kk >> 2) * (NPAD * 128) + (kk & 3) * 32) >> 4);
+        mma_ss_w(dS, sdesc_join(a_lo + oa, HI), sdesc_join(q_lo0 + ob, HI), IDESC_S,
+               kk > 0 ? 1u : 0u);
       }
-      if (ok) tc_commit(bar(C::B_OFULL));
-      // every issued MMA completes before tensor memory is released
-      tc_commit(bar(C::B_DONE));
-      wait_bar_drain(bar(C::B_DONE), 0u);
+      tc_commit_w(bar(C::B_EMPTY + st));
     }
+    if (ok) tc_commit_w(bar(C::B_SFULL));
+    for (int t = 0; ok && t < T; ++t) {
+      const int n = T + t, st = n % C::NS;
+      if (!wait_all(bar(C::B_FULL + st), (uint32_t)((n / C::NS) & 1), ctl) ||
+          !wait_all(bar(C::B_PFULL + (t & 1)), (uint32_t)((t >> 1) & 1), ctl)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t a_lo = v_lo0 + (uint32_t)(st * kTileBytes >> 4);
+      const uint32_t b_lo = p_lo0 + (uint32_t)((t & 1) * C::PB >> 4);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t oa = (uint32_t)((kk * 2048) >> 4);  // 16 keys x 128 bytes
+        const uint32_t ob = (uint32_t)(((kk >> 2) * (NPAD * 128) + (kk & 3) * 32) >> 4);
+        mma_ss_w(tmem, sdesc_join(a_lo + oa, HI), sdesc_join(b_lo + ob, HI), IDESC_O,
+               (t > 0 || kk > 0) ? 1u : 0u);
+      }
+      tc_commit_w(bar(C::B_EMPTY + st));
+      tc_commit_w(bar(C::B_PEMPTY + (t & 1)));
+    }
+    if (ok) tc_commit_w(bar(C::B_OFULL));
+    // every issued MMA completes before tensor memory is released
+    tc_commit_w(bar(C::B_DONE));
+    wait_bar_drain(bar(C::B_DONE), 0u);
+
   } else {
     // ======================================================= softmax (0-3)
     // Q rows into the B-operand layout: row c = query column (group head
