@@ -416,6 +416,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_tile<D>(sbase + C::K_OFF_K, &tmap_k, bar(C::KB_KVFULL), p.kperm, (int)j0, hk, b);
       tma_tile<D>(sbase + C::K_OFF_V, &tmap_v, bar(C::KB_KVFULL), p.vperm, (int)j0, hk, b);
     }
+    // LSE (log2 units) and D of a unit's 128 rows, 4 rows per lane; rows past
+    // Sq get P = 0.  They are loaded one unit ahead, so their latency
+    // overlaps the wait for the ring instead of holding back the unit's QFULL.
+    float nl[4], nd[4];
+    auto load_stats = [&](int u) {
+      const int g = u / per_g, m = m_first + u % per_g, h = hk * p.G + g;
+      const int64_t rb = ((int64_t)b * p.Hq + h) * p.Sq + (int64_t)m * 128;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int t = lane + 32 * k;
+        const bool in = (int64_t)m * 128 + t < p.Sq;
+        nl[k] = in ? p.lse[rb + t] * kLog2e : INFINITY;
+        nd[k] = in ? p.dsum[rb + t] : 0.f;
+      }
+    };
+    if (NU > 0) load_stats(0);
     int issued = 0;
     for (int u = 0; u < NU; ++u) {
       const int st = u % C::NS;
@@ -430,17 +446,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_tile<D>(sbase + C::K_OFF_DO + st * C::TILE, &tmap_do, bar(C::KB_QFULL + st), p.operm,
                     m * 128, h, b);
       }
-      // LSE (log2 units) and D of the tile's 128 rows; rows past Sq get P = 0
       float *sv = reinterpret_cast<float *>(smem + C::K_OFF_ST + st * 1024);
-      const int64_t rb = ((int64_t)b * p.Hq + h) * p.Sq + (int64_t)m * 128;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const int t = lane + 32 * k;
-        const bool in = (int64_t)m * 128 + t < p.Sq;
-        sv[t] = in ? p.lse[rb + t] * kLog2e : INFINITY;
-        sv[128 + t] = in ? p.dsum[rb + t] : 0.f;
+        sv[lane + 32 * k] = nl[k];
+        sv[128 + lane + 32 * k] = nd[k];
       }
       mbar_arrive(bar(C::KB_QFULL + st));
+      if (u + 1 < NU) load_stats(u + 1);
       issued = u + 1;
     }
     if (lane == 0) {  // copies in flight land before the block exits
