@@ -335,7 +335,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int m = m_first + u % per_g;
       ok = ok && __all_sync(0xffffffffu, wait_bar(bar(C::KB_QFULL + st), (uint32_t)((u / C::NS) & 1), ctl));
       ok = ok && __all_sync(0xffffffffu, wait_bar(bar(C::KB_SFULL), (uint32_t)(u & 1), ctl));
-      ok = ok && __all_sync(0xffffffffu, wait_bar(bar(C::KB_DPFULL), (uint32_t)(u & 1), ctl));
       if (!ok) break;
       tc_fence_after();
       const float4 *lse4 = reinterpret_cast<const float4 *>(smem + C::K_OFF_ST + st * 1024);
@@ -346,13 +345,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
       for (int bt = 0; bt < 2; ++bt) {
         const int c0 = 64 * hf + 32 * bt;  // query columns [c0, c0 + 32)
+        // P^T from S^T first: the exponentials of the first chunk overlap
+        // the dP^T products, which are only waited for before dS^T
         uint32_t sr[32], dr[32];
-        tmem_ld32_pair(lanes + 256u + (uint32_t)c0, lanes + 384u + (uint32_t)c0, sr, dr);
+        tmem_ld32(lanes + 256u + (uint32_t)c0, sr);
         uint32_t pp[16], pd[16];
 #pragma unroll
         for (int e4 = 0; e4 < 8; ++e4) {
-          const float4 l4 = lse4[(c0 >> 2) + e4], d4 = dsm4[(c0 >> 2) + e4];
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
+          const float4 l4 = lse4[(c0 >> 2) + e4];
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
           for (int k = 0; k < 4; k += 2) {
             const int e = 4 * e4 + k;
@@ -363,8 +364,27 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (c0 + e + 1 < lim) p1 = 0.f;
             }
             pp[e >> 1] = Pack16<TIn>::pack2(p0, p1);
-            pd[e >> 1] = f16x2(p0 * (__uint_as_float(dr[e]) - dv[k]),
-                               p1 * (__uint_as_float(dr[e + 1]) - dv[k + 1]));
+            sr[e] = __float_as_uint(p0);
+            sr[e + 1] = __float_as_uint(p1);
+          }
+        }
+        if (bt == 0) {
+          if (!__all_sync(0xffffffffu, wait_bar(bar(C::KB_DPFULL), (uint32_t)(u & 1), ctl))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        tmem_ld32(lanes + 384u + (uint32_t)c0, dr);
+#pragma unroll
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const float4 d4 = dsm4[(c0 >> 2) + e4];
+          const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+          for (int k = 0; k < 4; k += 2) {
+            const int e = 4 * e4 + k;
+            pd[e >> 1] = f16x2(__uint_as_float(sr[e]) * (__uint_as_float(dr[e]) - dv[k]),
+                               __uint_as_float(sr[e + 1]) * (__uint_as_float(dr[e + 1]) - dv[k + 1]));
           }
         }
         // packed into columns this warp has already read: [64 hf + 16 bt, +16)
@@ -372,6 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st16(lanes + 256u + pc, pp);
         tmem_st16(lanes + 384u + pc, pd);
       }
+      if (!ok) break;
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(C::KB_PFULL));
