@@ -628,36 +628,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int n = 0; n < N; ++n) {
       const int sl = n & 1;  // S slot of this key tile (TMEM cols 128 sl ..)
       ok = ok && __all_sync(0xffffffffu, wait_bar(bar(C::QB_SFULL + sl), (uint32_t)((n >> 1) & 1), ctl));
-      ok = ok && __all_sync(0xffffffffu, wait_bar(bar(C::QB_DPFULL), (uint32_t)(n & 1), ctl));
       if (!ok) break;
       tc_fence_after();
-      // dP first, then release its columns so the next tile's dP can start
-      uint32_t dr[64];
-      tmem_ld64(lanes + 256u + (uint32_t)(64 * hf), dr);
-      tc_fence_before();
-      mbar_arrive(bar(C::QB_DPFREE));
       const int64_t jt = (int64_t)n * 128;
       const bool straddle = (jt + 127 > p.off + i0) || (jt + 127 >= p.Sk);
       // key column c is admissible iff c <= lim
       const int64_t lim = min(qpos, p.Sk - 1) - jt;
       const uint32_t sbase_t = lanes + (uint32_t)(128 * sl);
+      // P from S first (kept in the S registers): the exponentials overlap
+      // the dP product, which is only waited for before dS
       uint32_t sr[64];
       tmem_ld64(sbase_t + (uint32_t)(64 * hf), sr);
 #pragma unroll
+      for (int x = 0; x < 64; x += 2) {
+        const int c = 64 * hf + x;
+        float p0 = ex2(fmaf(__uint_as_float(sr[x]), sl2, -lse2));
+        float p1 = ex2(fmaf(__uint_as_float(sr[x + 1]), sl2, -lse2));
+        if (straddle) {
+          if (c > lim) p0 = 0.f;
+          if (c + 1 > lim) p1 = 0.f;
+        }
+        sr[x] = __float_as_uint(p0);
+        sr[x + 1] = __float_as_uint(p1);
+      }
+      ok = __all_sync(0xffffffffu, wait_bar(bar(C::QB_DPFULL), (uint32_t)(n & 1), ctl));
+      if (!ok) break;
+      tc_fence_after();
+      // dP, then release its columns so the next tile's dP can start
+      uint32_t dr[64];
+      tmem_ld64(lanes + 256u + (uint32_t)(64 * hf), dr);
+      tc_fence_before();
+      mbar_arrive(bar(C::QB_DPFREE));
+#pragma unroll
       for (int bt = 0; bt < 2; ++bt) {
-        const int c0 = 64 * hf + 32 * bt;  // key columns [c0, c0 + 32)
         uint32_t pd[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const int x = 32 * bt + e;
-          float p0 = ex2(fmaf(__uint_as_float(sr[x]), sl2, -lse2));
-          float p1 = ex2(fmaf(__uint_as_float(sr[x + 1]), sl2, -lse2));
-          if (straddle) {
-            if (c0 + e > lim) p0 = 0.f;
-            if (c0 + e + 1 > lim) p1 = 0.f;
-          }
-          pd[e >> 1] = f16x2(p0 * (__uint_as_float(dr[x]) - dsum),
-                             p1 * (__uint_as_float(dr[x + 1]) - dsum));
+          pd[e >> 1] = f16x2(__uint_as_float(sr[x]) * (__uint_as_float(dr[x]) - dsum),
+                             __uint_as_float(sr[x + 1]) * (__uint_as_float(dr[x + 1]) - dsum));
         }
         // packed into columns this warp has already read: [64 hf + 16 bt, +16)
         tmem_st16(sbase_t + (uint32_t)(64 * hf + 16 * bt), pd);
