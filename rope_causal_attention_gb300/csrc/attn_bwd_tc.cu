@@ -37,13 +37,18 @@
 //   store in the input dtype.  A shared-memory tile in the 128-byte swizzled
 //   K-major layout doubles as the MN-major operand of the transposed product,
 //   so each operand tile is loaded once.
-// Roles (320 threads): warps 0-7 compute P and dS, two warps per TMEM lane
-// quadrant, each on half of the 128 columns (the half-warps pack their
-// 16-bit results into columns they have already read: +0 for the first half,
-// +64 for the second, and the TS products address the two halves per
-// k-step); warp 8 issues the TMA loads (and, for dK/dV, stages the row
-// statistics); warp 9 allocates TMEM and issues the MMAs.  Every mbarrier
-// wait is bounded (RA_ERR_DEVICE_TIMEOUT, abort flag, drain).
+// Roles.  dQ (320 threads): warps 0-7 compute P and dS, two warps per TMEM
+// lane quadrant, each on half of the 128 columns (they pack their 16-bit
+// results into columns they have already read: +0 for the first half, +64
+// for the second, and the TS products address the two halves per k-step);
+// warp 8 issues the TMA loads; warp 9 allocates TMEM and issues the MMAs.
+// dK/dV (576 threads): warps 0-15 compute P^T and dS^T, four warps per lane
+// quadrant, each on a quarter of the 128 query columns (P^T and dS^T packed
+// over the first 16 columns of the warp's own S^T and dP^T columns); warp 16
+// issues the TMA loads and stages the row statistics (one unit ahead);
+// warp 17 allocates TMEM and issues the MMAs.  The MMA warps issue
+// warp-wide (one elected lane per instruction).  Every mbarrier wait is
+// bounded (RA_ERR_DEVICE_TIMEOUT, abort flag, drain).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -61,8 +66,12 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 320;  // dQ: 8 compute warps, TMA, MMA
 constexpr int kWarpTma = 8, kWarpMma = 9;
+// dK/dV: 16 compute warps (4 per SM sub-partition: each owns 32 of the 128
+// query columns of a unit), then the TMA and MMA warps
+constexpr int kThreadsK = 576;
+constexpr int kWarpTmaK = 16, kWarpMmaK = 17;
 constexpr uint32_t kTmemCols = 512;
 constexpr long long kTimeoutCycles = 1LL << 32;  // about two seconds
 constexpr float kLog2e = 1.4426950408889634f;
@@ -267,7 +276,7 @@ __global__ void __launch_bounds__(256) bwd_rotate_f16_kernel(const TIn *__restri
 
 // ===================================================================== dK, dV
 template <int D, typename TIn>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsK, 1)
     bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                        const __grid_constant__ CUtensorMap tmap_k,
                        const __grid_constant__ CUtensorMap tmap_v,
@@ -301,17 +310,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(C::KB_SFULL), 1);
     mbar_init(bar(C::KB_DPFULL), 1);
-    mbar_init(bar(C::KB_PFULL), 256);
+    mbar_init(bar(C::KB_PFULL), 512);
     mbar_init(bar(C::KB_ACC), 1);
     mbar_init(bar(C::KB_DONE), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kWarpMma) {
+  if (warp == kWarpMmaK) {
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-  if (warp == kWarpTma && lane == 0) {
+  if (warp == kWarpTmaK && lane == 0) {
     prefetch_tmap(&tmap_q);
     prefetch_tmap(&tmap_k);
     prefetch_tmap(&tmap_v);
@@ -322,13 +331,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp < 8) {
+  if (warp < 16) {
     // ========================================================= P^T and dS^T
-    const int qd = warp & 3, hf = warp >> 2;
+    const int qd = warp & 3, cq = warp >> 2;  // TMEM lane quarter, query-column quarter
     const int t = qd * 32 + lane;  // key row of the tile = TMEM lane
     const uint32_t lanes = tmem + ((uint32_t)(qd * 32) << 16);
     const int64_t j = j0 + t;
     const float sl2 = p.scale_log2;
+    const int c0 = 32 * cq;  // query columns [c0, c0 + 32) of every unit
     bool ok = true;
     for (int u = 0; u < NU; ++u) {
       const int st = u % C::NS;
@@ -342,14 +352,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t i0 = (int64_t)m * 128;
       const bool straddle = j0 + 127 > p.off + i0;
       const int64_t lim = j - p.off - i0;  // query column c sees key j iff c >= lim
-#pragma unroll 1
-      for (int bt = 0; bt < 2; ++bt) {
-        const int c0 = 64 * hf + 32 * bt;  // query columns [c0, c0 + 32)
-        // P^T from S^T first: the exponentials of the first chunk overlap
-        // the dP^T products, which are only waited for before dS^T
-        uint32_t sr[32], dr[32];
-        tmem_ld32(lanes + 256u + (uint32_t)c0, sr);
-        uint32_t pp[16], pd[16];
+      // P^T from S^T first: the exponentials overlap the dP^T products,
+      // which are only waited for before dS^T
+      uint32_t sr[32], dr[32];
+      tmem_ld32(lanes + 256u + (uint32_t)c0, sr);
+      {
+        uint32_t pp[16];
 #pragma unroll
         for (int e4 = 0; e4 < 8; ++e4) {
           const float4 l4 = lse4[(c0 >> 2) + e4];
@@ -368,37 +376,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             sr[e + 1] = __float_as_uint(p1);
           }
         }
-        if (bt == 0) {
-          if (!__all_sync(0xffffffffu, wait_bar(bar(C::KB_DPFULL), (uint32_t)(u & 1), ctl))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-        }
-        tmem_ld32(lanes + 384u + (uint32_t)c0, dr);
-#pragma unroll
-        for (int e4 = 0; e4 < 8; ++e4) {
-          const float4 d4 = dsm4[(c0 >> 2) + e4];
-          const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-#pragma unroll
-          for (int k = 0; k < 4; k += 2) {
-            const int e = 4 * e4 + k;
-            pd[e >> 1] = f16x2(__uint_as_float(sr[e]) * (__uint_as_float(dr[e]) - dv[k]),
-                               __uint_as_float(sr[e + 1]) * (__uint_as_float(dr[e + 1]) - dv[k + 1]));
-          }
-        }
-        // packed into columns this warp has already read: [64 hf + 16 bt, +16)
-        const uint32_t pc = (uint32_t)(64 * hf + 16 * bt);
-        tmem_st16(lanes + 256u + pc, pp);
-        tmem_st16(lanes + 384u + pc, pd);
+        // P^T packed over the first 16 of the S^T columns this warp has read
+        tmem_st16(lanes + 256u + (uint32_t)c0, pp);
       }
-      if (!ok) break;
+      if (!__all_sync(0xffffffffu, wait_bar(bar(C::KB_DPFULL), (uint32_t)(u & 1), ctl))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      tmem_ld32(lanes + 384u + (uint32_t)c0, dr);
+      uint32_t pd[16];
+#pragma unroll
+      for (int e4 = 0; e4 < 8; ++e4) {
+        const float4 d4 = dsm4[(c0 >> 2) + e4];
+        const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+        for (int k = 0; k < 4; k += 2) {
+          const int e = 4 * e4 + k;
+          pd[e >> 1] = f16x2(__uint_as_float(sr[e]) * (__uint_as_float(dr[e]) - dv[k]),
+                             __uint_as_float(sr[e + 1]) * (__uint_as_float(dr[e + 1]) - dv[k + 1]));
+        }
+      }
+      // dS^T packed over the first 16 of the dP^T columns this warp has read
+      tmem_st16(lanes + 384u + (uint32_t)c0, pd);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(C::KB_PFULL));
     }
     // ---- epilogue: dV straight from TMEM; dK = R(j)^T (scale dK~) through a
-    // padded fp32 row per key (the rotation pairs dims across the halves)
+    // padded fp32 row per key (the rotation pairs dims across the quarters)
     const bool acc = ok && NU > 0 &&
                      __all_sync(0xffffffffu, wait_bar(bar(C::KB_ACC), 0u, ctl));
     const bool write = ok && (NU == 0 || acc);
@@ -407,16 +413,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     TIn *dvd = static_cast<TIn *>(p.dv) + b * p.sdv0 + hk * p.sdv1 + j * p.sdv2;
     TIn *dkd = static_cast<TIn *>(p.dk) + b * p.sdk0 + hk * p.sdk1 + j * p.sdk2;
     const bool row_ok = j < p.Sk;
-    constexpr int HD = D / 2;  // dims per half-warp
+    constexpr int QD = D / 4;  // dims per column quarter
 #pragma unroll 1
-    for (int c = 0; c < HD / 32; ++c) {
-      const int col = HD * hf + 32 * c;
-      uint32_t r[32];
-      if (acc) tmem_ld32(lanes + (uint32_t)col, r);
+    for (int c = 0; c < QD / 16; ++c) {
+      const int col = QD * cq + 16 * c;
+      uint32_t r[16];
+      if (acc) tmem_ld16(lanes + (uint32_t)col, r);
       if (write && row_ok) {
         uint4 *d4 = reinterpret_cast<uint4 *>(dvd + col);
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
+        for (int g = 0; g < 2; ++g) {
           float v[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) v[e] = acc ? __uint_as_float(r[8 * g + e]) : 0.f;
@@ -424,13 +430,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                              Pack16<TIn>::pack2(v[4], v[5]), Pack16<TIn>::pack2(v[6], v[7]));
         }
       }
-      if (acc) tmem_ld32(lanes + (uint32_t)(D + col), r);
+      if (acc) tmem_ld16(lanes + (uint32_t)(D + col), r);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) row[col + e] = acc ? __uint_as_float(r[e]) * p.scale : 0.f;
+      for (int e = 0; e < 16; ++e) row[col + e] = acc ? __uint_as_float(r[e]) * p.scale : 0.f;
     }
-    named_bar_sync(1, 256);  // both halves of every row are in shared memory
-    if (write && row_ok) store_row<D, TIn>(row, true, j, dkd, hf * (D / 16), (hf + 1) * (D / 16), p);
-  } else if (warp == kWarpTma) {
+    named_bar_sync(1, 512);  // all quarters of every row are in shared memory
+    if (write && row_ok) store_row<D, TIn>(row, true, j, dkd, cq * (D / 32), (cq + 1) * (D / 32), p);
+  } else if (warp == kWarpTmaK) {
     // ============================================= TMA and row statistics
     if (lane == 0) {
       mbar_arrive_expect_tx(bar(C::KB_KVFULL), (uint32_t)(2 * C::TILE));
@@ -525,15 +531,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      // 16 queries per step; queries 64..127 were packed at column +64
+      // 16 queries per step: query block kk is in column quarter kk / 2, 8 packed columns per half
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_ts_w(tmem, tmem + 256u + (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8),
+        mma_ts_w(tmem, tmem + 256u + (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8),
                sdesc_join(domn_lo0 + so + (uint32_t)(kk * 2048 >> 4), HI), IDESC_DV,
                (u > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_ts_w(tmem + (uint32_t)D, tmem + 384u + (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8),
+        mma_ts_w(tmem + (uint32_t)D, tmem + 384u + (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8),
                sdesc_join(qmn_lo0 + so + (uint32_t)(kk * 2048 >> 4), HI), IDESC_DK,
                (u > 0 || kk > 0) ? 1u : 0u);
       tc_commit_w(bar(C::KB_QEMPTY + st));
@@ -546,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == kWarpMma) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kWarpMmaK) tmem_dealloc(tmem, kTmemCols);
 }
 
 // ========================================================================= dQ
@@ -860,7 +866,7 @@ cudaError_t launch_typed(const CUtensorMap (&maps)[4], const BwdTcParams &p, cud
   const int64_t gk = (int64_t)p.n_kt * p.B * p.Hkv;
   const int64_t gq = (int64_t)p.n_qt * p.B * p.Hq;
   if (gk > 0x7fffffff || gq > 0x7fffffff) return cudaErrorInvalidConfiguration;
-  bwd_dkdv_tc_kernel<D, TIn><<<(unsigned)gk, kThreads, C::K_SMEM, s>>>(maps[0], maps[1], maps[2],
+  bwd_dkdv_tc_kernel<D, TIn><<<(unsigned)gk, kThreadsK, C::K_SMEM, s>>>(maps[0], maps[1], maps[2],
                                                                        maps[3], p);
   note_launch("bwd_dkdv_tc_kernel");
   cudaError_t e = cudaGetLastError();
