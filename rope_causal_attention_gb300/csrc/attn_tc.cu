@@ -20,9 +20,10 @@
 //   warps 8-11  rotation: Q tiles once, then each K tile as it is staged:
 //               global bf16/fp16 -> fp32 rotation with the fp32 cos/sin table
 //               -> fp16 operand in 128B-swizzled shared memory
-//   warp 12     TMA producer for V tiles (raw, never rotated)
+//   warp 12     TMA producer for raw K tiles (into their operand stages)
 //   warp 13     tcgen05 MMA issuer; owns the tensor-memory allocation
-//   warps 14-15 idle (complete the fourth warpgroup)
+//   warp 14     TMA producer for V tiles (raw, never rotated)
+//   warp 15     idle (completes the fourth warpgroup)
 // Tensor memory (512 columns): S0 | S1 | O0 | O1.  P is written as 16-bit
 // pairs over the first 64 columns of its S block and fed to the PV product
 // straight from tensor memory.  The issue order S0(n+1) after PV0(n) and
@@ -55,36 +56,42 @@ using namespace ptx;
 
 constexpr int kThreads = 512;  // four full warpgroups
 constexpr int kWarpRot = 8;
-constexpr int kWarpTma = 12;
+constexpr int kWarpTma = 12;   // K tiles
+constexpr int kWarpTmaV = 14;  // V tiles: its own warp, so K loads run ahead of V's ring
 constexpr int kWarpMma = 13;
 constexpr uint32_t kTmemCols = 512;
 constexpr long long kTimeoutCycles = 1LL << 32;  // about two seconds
 
 template <int D>
 struct TcCfg {
-  static constexpr int NS = (D == 128) ? 2 : 3;  // K~ and V pipeline stages
+  // K~ and V pipeline stages.  A K stage is held from its TMA load through
+  // the in-place rotation to the last S product that reads it, so K gets
+  // the deeper ring; at D = 128 the third K stage fills shared memory.
+  static constexpr int NSK = 3;
+  static constexpr int NSV = (D == 128) ? 2 : 3;
   static constexpr int TILE = 128 * D * 2;       // one 128-row tile of 16-bit values
   static constexpr int SUBT = 128 * 128;         // one 64-column (128-byte-row) sub-tile
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = 2 * TILE;
-  static constexpr int OFF_V = OFF_K + NS * TILE;
-  static constexpr int OFF_BAR = OFF_V + NS * TILE;
+  static constexpr int OFF_V = OFF_K + NSK * TILE;
+  static constexpr int OFF_BAR = OFF_V + NSV * TILE;
   static constexpr int B_QFULL = 0;
   static constexpr int B_KFULL = 2;
-  static constexpr int B_KEMPTY = 2 + NS;
-  static constexpr int B_VFULL = 2 + 2 * NS;
-  static constexpr int B_VEMPTY = 2 + 3 * NS;
-  static constexpr int B_SFULL = 2 + 4 * NS;
-  static constexpr int B_PFULL = 4 + 4 * NS;
-  static constexpr int B_OFULL = 6 + 4 * NS;
-  static constexpr int B_DONE = 8 + 4 * NS;
-  static constexpr int B_KRAW = 9 + 4 * NS;  // raw K tile landed (TMA), per stage
-  static constexpr int B_MERGE = 9 + 5 * NS;  // split blocks: slot 1's row statistics stored
-  static constexpr int NBAR = 10 + 5 * NS;
+  static constexpr int B_KEMPTY = B_KFULL + NSK;
+  static constexpr int B_VFULL = B_KEMPTY + NSK;
+  static constexpr int B_VEMPTY = B_VFULL + NSV;
+  static constexpr int B_SFULL = B_VEMPTY + NSV;
+  static constexpr int B_PFULL = B_SFULL + 2;
+  static constexpr int B_OFULL = B_PFULL + 2;
+  static constexpr int B_DONE = B_OFULL + 2;
+  static constexpr int B_KRAW = B_DONE + 1;  // raw K tile landed (TMA), per stage
+  static constexpr int B_MERGE = B_KRAW + NSK;  // split blocks: slot 1's row statistics stored
+  static constexpr int NBAR = B_MERGE + 1;
   // split blocks leave query buffer 1 unused; slot 1's (m, l) per row go there
   static constexpr int OFF_STATS = OFF_Q + TILE;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;  // slack to align the base to 1024
+  static_assert(SMEM <= 232448, "above the 227 KB of shared memory a block may opt into");
   // tensor-memory columns: S0 | S1 | O0 | O1
   static __device__ __forceinline__ uint32_t s_col(int slot) { return slot ? 128u : 0u; }
   static __device__ __forceinline__ uint32_t o_col(int slot) { return 256u + (slot ? D : 0); }
@@ -636,10 +643,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar(C::B_QFULL + 0), 128);
     mbar_init(bar(C::B_QFULL + 1), 128);
-    for (int i = 0; i < C::NS; ++i) {
+    for (int i = 0; i < C::NSK; ++i) {
       mbar_init(bar(C::B_KRAW + i), 1);
       mbar_init(bar(C::B_KFULL + i), 128);
       mbar_init(bar(C::B_KEMPTY + i), 1);
+    }
+    for (int i = 0; i < C::NSV; ++i) {
       mbar_init(bar(C::B_VFULL + i), 1);
       mbar_init(bar(C::B_VEMPTY + i), 1);
     }
@@ -658,10 +667,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-  if (warp == kWarpTma && lane == 0) {
-    prefetch_tmap(&tmap_k);
-    prefetch_tmap(&tmap_v);
-  }
+  if (warp == kWarpTma && lane == 0) prefetch_tmap(&tmap_k);
+  if (warp == kWarpTmaV && lane == 0) prefetch_tmap(&tmap_v);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -839,15 +846,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = threadIdx.x - kWarpRot * 32;
     if (p.apply_rope && p.rot_dim == D) {
       if (p.layout == RA_NEOX)
-        rotate_k_loop<D, TIn, RA_NEOX, C::NS>(p, N, nend0, nend1, t, smem + C::OFF_K,
+        rotate_k_loop<D, TIn, RA_NEOX, C::NSK>(p, N, nend0, nend1, t, smem + C::OFF_K,
                                              bar(C::B_KRAW), bar(C::B_KFULL), ctl);
       else
-        rotate_k_loop<D, TIn, RA_GPTJ, C::NS>(p, N, nend0, nend1, t, smem + C::OFF_K,
+        rotate_k_loop<D, TIn, RA_GPTJ, C::NSK>(p, N, nend0, nend1, t, smem + C::OFF_K,
                                              bar(C::B_KRAW), bar(C::B_KFULL), ctl);
     } else {
       for (int n = 0; n < N; ++n) {
-        const int st = n % C::NS;
-        if (!wait_bar(bar(C::B_KRAW + st), (uint32_t)((n / C::NS) & 1), ctl)) break;
+        const int st = n % C::NSK;
+        if (!wait_bar(bar(C::B_KRAW + st), (uint32_t)((n / C::NSK) & 1), ctl)) break;
         const int64_t j = (int64_t)ktile(n) * 128 + t;
         if (j < p.Sk)  // rows past Sk were zero-filled by the TMA and stay zero
           rotate_row_inplace<D, TIn>(smem + C::OFF_K + st * C::TILE, t, j, p);
@@ -858,48 +865,55 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     setmaxnreg_to<128, kRegCtrl>();
     if (warp == kWarpTma) {
-      // ================================================================== TMA
+      // ================================================================ TMA K
       if (lane == 0) {
-        int issued = 0, k_issued = 0;
-        const int first_real = p.withhold_v0 ? 1 : 0;  // V tiles below this are never loaded
+        int k_issued = 0;
         for (int n = 0; n < N; ++n) {
-          const int st = n % C::NS;
-          // raw K tile n into its operand stage, once S(n - NS) has read the old one
-          if (n >= C::NS &&
-              !wait_bar(bar(C::B_KEMPTY + st), (uint32_t)((n / C::NS - 1) & 1), ctl))
+          const int st = n % C::NSK;
+          // raw K tile n into its operand stage, once S(n - NSK) has read the old one
+          if (n >= C::NSK &&
+              !wait_bar(bar(C::B_KEMPTY + st), (uint32_t)((n / C::NSK - 1) & 1), ctl))
             break;
           const int kt = ktile(n);
           mbar_arrive_expect_tx(bar(C::B_KRAW + st), (uint32_t)C::TILE);
-          {
-            const int c1 = p.kperm[0] == 0 ? kt * 128 : (p.kperm[0] == 1 ? hk : b);
-            const int c2 = p.kperm[1] == 0 ? kt * 128 : (p.kperm[1] == 1 ? hk : b);
-            const int c3 = p.kperm[2] == 0 ? kt * 128 : (p.kperm[2] == 1 ? hk : b);
+          const int c1 = p.kperm[0] == 0 ? kt * 128 : (p.kperm[0] == 1 ? hk : b);
+          const int c2 = p.kperm[1] == 0 ? kt * 128 : (p.kperm[1] == 1 ? hk : b);
+          const int c3 = p.kperm[2] == 0 ? kt * 128 : (p.kperm[2] == 1 ? hk : b);
 #pragma unroll
-            for (int sub = 0; sub < D / 64; ++sub)
-              tma_load_4d(sbase + C::OFF_K + st * C::TILE + sub * C::SUBT, &tmap_k,
-                          bar(C::B_KRAW + st), sub * 64, c1, c2, c3);
-          }
+          for (int sub = 0; sub < D / 64; ++sub)
+            tma_load_4d(sbase + C::OFF_K + st * C::TILE + sub * C::SUBT, &tmap_k,
+                        bar(C::B_KRAW + st), sub * 64, c1, c2, c3);
           k_issued = n + 1;
-          if (n >= C::NS &&
-              !wait_bar(bar(C::B_VEMPTY + st), (uint32_t)((n / C::NS - 1) & 1), ctl))
+        }
+        if (*abort_flag)  // let copies already in flight land before the block exits
+          for (int n = max(0, k_issued - C::NSK); n < k_issued; ++n)
+            wait_bar_drain(bar(C::B_KRAW + n % C::NSK), (uint32_t)((n / C::NSK) & 1));
+      }
+    } else if (warp == kWarpTmaV) {
+      // ================================================================ TMA V
+      if (lane == 0) {
+        int issued = 0;
+        const int first_real = p.withhold_v0 ? 1 : 0;  // V tiles below this are never loaded
+        for (int n = 0; n < N; ++n) {
+          const int sv = n % C::NSV;
+          if (n >= C::NSV &&
+              !wait_bar(bar(C::B_VEMPTY + sv), (uint32_t)((n / C::NSV - 1) & 1), ctl))
             break;
           if (n < first_real) continue;
-          mbar_arrive_expect_tx(bar(C::B_VFULL + st), (uint32_t)C::TILE);
+          const int kt = ktile(n);
+          mbar_arrive_expect_tx(bar(C::B_VFULL + sv), (uint32_t)C::TILE);
           const int c1 = p.vperm[0] == 0 ? kt * 128 : (p.vperm[0] == 1 ? hk : b);
           const int c2 = p.vperm[1] == 0 ? kt * 128 : (p.vperm[1] == 1 ? hk : b);
           const int c3 = p.vperm[2] == 0 ? kt * 128 : (p.vperm[2] == 1 ? hk : b);
 #pragma unroll
           for (int sub = 0; sub < D / 64; ++sub)
-            tma_load_4d(sbase + C::OFF_V + st * C::TILE + sub * C::SUBT, &tmap_v,
-                        bar(C::B_VFULL + st), sub * 64, c1, c2, c3);
+            tma_load_4d(sbase + C::OFF_V + sv * C::TILE + sub * C::SUBT, &tmap_v,
+                        bar(C::B_VFULL + sv), sub * 64, c1, c2, c3);
           issued = n + 1;
         }
-        if (*abort_flag) {  // let copies already in flight land before the block exits
-          for (int n = max(0, k_issued - C::NS); n < k_issued; ++n)
-            wait_bar_drain(bar(C::B_KRAW + n % C::NS), (uint32_t)((n / C::NS) & 1));
-          for (int n = max(first_real, issued - C::NS); n < issued; ++n)
-            wait_bar_drain(bar(C::B_VFULL + n % C::NS), (uint32_t)((n / C::NS) & 1));
-        }
+        if (*abort_flag)
+          for (int n = max(first_real, issued - C::NSV); n < issued; ++n)
+            wait_bar_drain(bar(C::B_VFULL + n % C::NSV), (uint32_t)((n / C::NSV) & 1));
       }
     } else if (warp == kWarpMma) {
       // ================================================================== MMA
@@ -939,8 +953,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = wait_all(bar(C::B_QFULL + 0), 0u, ctl);
         for (int s = 0; ok && s < 2; ++s) {
           if (!part(s, 0)) continue;
-          const int e = split_entry(s, 0, nend1), st = e % C::NS;
-          if (!wait_all(bar(C::B_KFULL + st), (uint32_t)((e / C::NS) & 1), ctl)) { ok = false; break; }
+          const int e = split_entry(s, 0, nend1), st = e % C::NSK;
+          if (!wait_all(bar(C::B_KFULL + st), (uint32_t)((e / C::NSK) & 1), ctl)) { ok = false; break; }
           mma_s(s, st);
           tc_commit_w(bar(C::B_SFULL + s));
           tc_commit_w(bar(C::B_KEMPTY + st));
@@ -948,8 +962,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int n = 0; ok && n < nend0; ++n) {
           for (int s = 0; s < 2; ++s) {
             if (!part(s, n)) continue;
-            const int e = split_entry(s, n, nend1), st = e % C::NS;
-            if (!wait_all(bar(C::B_VFULL + st), (uint32_t)((e / C::NS) & 1), ctl) ||
+            const int e = split_entry(s, n, nend1), st = e % C::NSV;
+            if (!wait_all(bar(C::B_VFULL + st), (uint32_t)((e / C::NSV) & 1), ctl) ||
                 !wait_all(bar(C::B_PFULL + s), (uint32_t)(n & 1), ctl)) {
               ok = false;
               break;
@@ -961,8 +975,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_commit_w(bar(C::B_OFULL + s));
               continue;
             }
-            const int e2 = split_entry(s, n + 1, nend1), st2 = e2 % C::NS;
-            if (!wait_all(bar(C::B_KFULL + st2), (uint32_t)((e2 / C::NS) & 1), ctl)) {
+            const int e2 = split_entry(s, n + 1, nend1), st2 = e2 % C::NSK;
+            if (!wait_all(bar(C::B_KFULL + st2), (uint32_t)((e2 / C::NSK) & 1), ctl)) {
               ok = false;
               break;
             }
@@ -984,8 +998,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_commit_w(bar(C::B_KEMPTY + 0));
         }
         for (int n = 0; ok && n < N; ++n) {
-          const int st = n % C::NS, nst = (n + 1) % C::NS;
-          if (!wait_all(bar(C::B_VFULL + st), (uint32_t)((n / C::NS) & 1), ctl)) { ok = false; break; }
+          const int st = n % C::NSV, nst = (n + 1) % C::NSK;
+          if (!wait_all(bar(C::B_VFULL + st), (uint32_t)((n / C::NSV) & 1), ctl)) { ok = false; break; }
           bool k_next = false;
           for (int s = 0; s < 2; ++s) {
             if (!part(s, n)) continue;
@@ -995,7 +1009,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (n == (s ? nend1 : nend0) - 1) tc_commit_w(bar(C::B_OFULL + s));
             if (part(s, n + 1)) {
               if (!k_next) {
-                if (!wait_all(bar(C::B_KFULL + nst), (uint32_t)(((n + 1) / C::NS) & 1), ctl)) {
+                if (!wait_all(bar(C::B_KFULL + nst), (uint32_t)(((n + 1) / C::NSK) & 1), ctl)) {
                   ok = false;
                   break;
                 }
