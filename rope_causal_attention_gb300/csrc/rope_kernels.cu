@@ -17,7 +17,9 @@
 // within the block, so a warp touches consecutive slices of consecutive heads
 // -- contiguous 128-bit accesses.  A thread issues all its heads' loads before
 // its first store, and loads the token's cos/sin slice once (read-only path)
-// for all of them; Q and K heads share one launch.
+// for all of them; Q and K heads share one launch.  Q/K rows are read and
+// written with the streaming (evict-first) cache hint: each is touched once,
+// so they should not displace the cos/sin rows that nearby tokens share.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -97,8 +99,8 @@ __global__ void __launch_bounds__(512) rope_apply_vec_kernel(RopeKParams p) {
 #pragma unroll
     for (int k = 0; k < NH; ++k) {
       if (!ok[k] || !(rot_slice || tail_slice)) continue;
-      raw[k][0] = *reinterpret_cast<const uint4 *>(src[k] + off0);
-      if (LD == 2 && rot_slice) raw[k][LD - 1] = *reinterpret_cast<const uint4 *>(src[k] + off1);
+      raw[k][0] = __ldcs(reinterpret_cast<const uint4 *>(src[k] + off0));
+      if (LD == 2 && rot_slice) raw[k][LD - 1] = __ldcs(reinterpret_cast<const uint4 *>(src[k] + off1));
     }
     const int64_t pos = load_position(p.positions, p.is64, t);
     if (pos < 0 || pos >= p.table_rows) {
@@ -121,8 +123,8 @@ __global__ void __launch_bounds__(512) rope_apply_vec_kernel(RopeKParams p) {
             olo[j] = lo[j] * c[j] - hi[j] * sn[j];
             ohi[j] = hi[j] * c[j] + lo[j] * sn[j];
           }
-          *reinterpret_cast<uint4 *>(dst[k] + off0) = pack16<T>(olo);
-          *reinterpret_cast<uint4 *>(dst[k] + off1) = pack16<T>(ohi);
+          __stcs(reinterpret_cast<uint4 *>(dst[k] + off0), pack16<T>(olo));
+          __stcs(reinterpret_cast<uint4 *>(dst[k] + off1), pack16<T>(ohi));
         } else {
           float x[V], y[V];
           unpack16<T>(raw[k][0], x);
@@ -131,13 +133,13 @@ __global__ void __launch_bounds__(512) rope_apply_vec_kernel(RopeKParams p) {
             y[2 * j] = x[2 * j] * c[j] - x[2 * j + 1] * sn[j];
             y[2 * j + 1] = x[2 * j + 1] * c[j] + x[2 * j] * sn[j];
           }
-          *reinterpret_cast<uint4 *>(dst[k] + off0) = pack16<T>(y);
+          __stcs(reinterpret_cast<uint4 *>(dst[k] + off0), pack16<T>(y));
         }
       }
     } else if (tail_slice) {  // out of place: copy the unrotated tail
 #pragma unroll
       for (int k = 0; k < NH; ++k)
-        if (ok[k]) *reinterpret_cast<uint4 *>(dst[k] + off0) = raw[k][0];
+        if (ok[k]) __stcs(reinterpret_cast<uint4 *>(dst[k] + off0), raw[k][0]);
     }
   }
 }
