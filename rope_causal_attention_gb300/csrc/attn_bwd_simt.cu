@@ -69,6 +69,36 @@ __device__ __forceinline__ float rot_at(const float *x, int d, int64_t pos, floa
   return low ? x[d] * c - x[partner] * s : x[d] * c + x[partner] * s;
 }
 
+// D_i = <dO_i, O_i> with 16-byte loads: CH = D / (16 / sizeof(T)) lanes per
+// row (a power of two <= 32), 32 / CH rows per warp; O and dO are read once,
+// so they take the streaming cache hint.
+template <typename T>
+__global__ void __launch_bounds__(256) bwd_rowterm_vec_kernel(const T *o, const T *dout,
+                                                              float *dsum, int Hq, int64_t Sq,
+                                                              int CH, int64_t so0, int64_t so1,
+                                                              int64_t so2, int64_t sd0,
+                                                              int64_t sd1, int64_t sd2,
+                                                              int64_t rows) {
+  constexpr int V = VecN<T>::N;
+  const int lane = threadIdx.x & 31;
+  const int c = lane & (CH - 1);
+  const int64_t r = ((int64_t)blockIdx.x * 8 + (threadIdx.x >> 5)) * (32 / CH) + lane / CH;
+  float acc = 0.f;
+  if (r < rows) {
+    const int64_t i = r % Sq, bh = r / Sq;
+    const int64_t h = bh % Hq, b = bh / Hq;
+    const uint4 uo = __ldcs(reinterpret_cast<const uint4 *>(o + b * so0 + h * so1 + i * so2) + c);
+    const uint4 ud = __ldcs(reinterpret_cast<const uint4 *>(dout + b * sd0 + h * sd1 + i * sd2) + c);
+    float fo[V], fd[V];
+    unpack16<T>(uo, fo);
+    unpack16<T>(ud, fd);
+#pragma unroll
+    for (int e = 0; e < V; ++e) acc = fmaf(fo[e], fd[e], acc);
+  }
+  for (int off = CH >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (c == 0 && r < rows) dsum[r] = acc;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) bwd_rowterm_kernel(const T *o, const T *dout, float *dsum,
                                                           int Hq, int64_t Sq, int D, int64_t so0,
@@ -287,6 +317,23 @@ BwdSimtParams simt_params(const BwdArgs &a) {
 template <typename T>
 cudaError_t rowterm_typed(const BwdArgs &a, cudaStream_t s) {
   const int64_t rows = (int64_t)a.f.B * a.f.Hq * a.f.Sq;
+  constexpr int V = VecN<T>::N;
+  const int CH = a.f.D / V;  // lanes per row in the vector kernel
+  // the vector kernel serves the 16-bit inputs of the tensor-core backward
+  bool vec = sizeof(T) == 2 && a.f.D % V == 0 && CH >= 1 && CH <= 32 && (CH & (CH - 1)) == 0 &&
+             reinterpret_cast<uintptr_t>(a.o) % 16 == 0 &&
+             reinterpret_cast<uintptr_t>(a.dout) % 16 == 0;
+  for (int j = 0; j < 3; ++j) vec = vec && a.sod[j] % V == 0 && a.sdo[j] % V == 0;
+  if (vec) {
+    const int64_t rows_per_block = 8 * (32 / CH);
+    const int64_t blocks = (rows + rows_per_block - 1) / rows_per_block;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    bwd_rowterm_vec_kernel<T><<<(unsigned)blocks, 256, 0, s>>>(
+        static_cast<const T *>(a.o), static_cast<const T *>(a.dout), a.dsum, a.f.Hq, a.f.Sq,
+        CH, a.sod[0], a.sod[1], a.sod[2], a.sdo[0], a.sdo[1], a.sdo[2], rows);
+    note_launch("bwd_rowterm_vec_kernel");
+    return cudaGetLastError();
+  }
   const int64_t blocks = (rows + 7) / 8;
   if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
   bwd_rowterm_kernel<T><<<(unsigned)blocks, 256, 0, s>>>(

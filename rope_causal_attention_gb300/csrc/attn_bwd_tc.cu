@@ -222,9 +222,25 @@ __device__ __forceinline__ void store_row(const float *row, bool rotate, int64_t
 
 // ================================================================ rotation
 // Rotated fp16 copy of a [B][H][S][D] tensor (row s at position pos0 + s),
-// written contiguous: one thread per 16-byte output chunk (NeoX: a chunk of
-// the low half together with its high-half partner; GPT-J: four pairs);
-// fp32 arithmetic with the fp32 table, one rounding to fp16.
+// written contiguous.  A row's work items are its rotation units (NeoX: a
+// 16-byte chunk of the low half with its high-half partner; GPT-J: a 16-byte
+// chunk of whole pairs), then the 16-byte chunks of the unrotated tail;
+// without rotation every chunk is a tail chunk.  One thread per item: fp32
+// arithmetic with the fp32 table (float4 loads: the host passes 16-byte
+// aligned tables and whole 8-element units), one rounding to fp16.  The
+// input is read once, with the streaming cache hint.
+__host__ __device__ inline int rotate_units(int D, int apply_rope, int rot_dim, int layout) {
+  if (!apply_rope) return D >> 3;
+  return (layout == RA_NEOX ? rot_dim >> 4 : rot_dim >> 3) + ((D - rot_dim) >> 3);
+}
+
+__device__ __forceinline__ void ld_f4x2(const float *p, float *f) {
+  const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+  const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
 template <typename TIn>
 __global__ void __launch_bounds__(256) bwd_rotate_f16_kernel(const TIn *__restrict__ x, int H,
                                                              int64_t S, int D, int64_t s0,
@@ -233,43 +249,50 @@ __global__ void __launch_bounds__(256) bwd_rotate_f16_kernel(const TIn *__restri
                                                              int apply_rope, int rot_dim,
                                                              int layout, const float *cos_t,
                                                              const float *sin_t, int64_t n) {
-  const int NC = D >> 3;  // chunks per row
+  const int half = rot_dim >> 1;
+  const int per_row = rotate_units(D, apply_rope, rot_dim, layout);
+  const int nr = apply_rope ? (layout == RA_NEOX ? rot_dim >> 4 : rot_dim >> 3) : 0;
+  const int tail0 = apply_rope ? rot_dim >> 3 : 0;  // first tail chunk
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n;
        idx += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = idx / NC;
-    const int c = (int)(idx - r * NC);
+    const int64_t r = idx / per_row;
+    const int u = (int)(idx - r * per_row);
     const int64_t s = r % S, h = (r / S) % H, b = r / (S * H);
     const TIn *src = x + b * s0 + h * s1 + s * s2;
     __half *dst = out + r * D;
-    const int half = rot_dim >> 1;
-    float a[8];
-    unpack16<TIn>(*reinterpret_cast<const uint4 *>(src + 8 * c), a);
-    if (!apply_rope || 8 * c >= rot_dim) {
+    if (u >= nr) {  // a chunk of the unrotated tail
+      const int c = tail0 + (u - nr);
+      float a[8];
+      unpack16<TIn>(__ldcs(reinterpret_cast<const uint4 *>(src + 8 * c)), a);
       *reinterpret_cast<uint4 *>(dst + 8 * c) = pack16<__half>(a);
       continue;
     }
     const float *cr = cos_t + (pos0 + s) * half, *sr = sin_t + (pos0 + s) * half;
     if (layout == RA_NEOX) {
-      if (8 * c >= half) continue;  // written by the low-half partner
-      float hb[8], lo[8], hi[8];
-      unpack16<TIn>(*reinterpret_cast<const uint4 *>(src + 8 * c + half), hb);
+      float lo[8], hi[8], cs[8], sn[8], a[8], bb[8];
+      unpack16<TIn>(__ldcs(reinterpret_cast<const uint4 *>(src + 8 * u)), lo);
+      unpack16<TIn>(__ldcs(reinterpret_cast<const uint4 *>(src + 8 * u + half)), hi);
+      ld_f4x2(cr + 8 * u, cs);
+      ld_f4x2(sr + 8 * u, sn);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const float cs = __ldg(cr + 8 * c + e), sn = __ldg(sr + 8 * c + e);
-        lo[e] = a[e] * cs - hb[e] * sn;
-        hi[e] = hb[e] * cs + a[e] * sn;
+        a[e] = lo[e] * cs[e] - hi[e] * sn[e];
+        bb[e] = hi[e] * cs[e] + lo[e] * sn[e];
       }
-      *reinterpret_cast<uint4 *>(dst + 8 * c) = pack16<__half>(lo);
-      *reinterpret_cast<uint4 *>(dst + 8 * c + half) = pack16<__half>(hi);
+      *reinterpret_cast<uint4 *>(dst + 8 * u) = pack16<__half>(a);
+      *reinterpret_cast<uint4 *>(dst + 8 * u + half) = pack16<__half>(bb);
     } else {
-      float y[8];
+      float xv[8], y[8];
+      unpack16<TIn>(__ldcs(reinterpret_cast<const uint4 *>(src + 8 * u)), xv);
+      const float4 cs = __ldg(reinterpret_cast<const float4 *>(cr + 4 * u));
+      const float4 sn = __ldg(reinterpret_cast<const float4 *>(sr + 4 * u));
+      const float c4[4] = {cs.x, cs.y, cs.z, cs.w}, s4[4] = {sn.x, sn.y, sn.z, sn.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float cs = __ldg(cr + 4 * c + e), sn = __ldg(sr + 4 * c + e);
-        y[2 * e] = a[2 * e] * cs - a[2 * e + 1] * sn;
-        y[2 * e + 1] = a[2 * e + 1] * cs + a[2 * e] * sn;
+        y[2 * e] = xv[2 * e] * c4[e] - xv[2 * e + 1] * s4[e];
+        y[2 * e + 1] = xv[2 * e + 1] * c4[e] + xv[2 * e] * s4[e];
       }
-      *reinterpret_cast<uint4 *>(dst + 8 * c) = pack16<__half>(y);
+      *reinterpret_cast<uint4 *>(dst + 8 * u) = pack16<__half>(y);
     }
   }
 }
@@ -838,7 +861,7 @@ cudaError_t make_rows_map(const void *base, int B, int H, int64_t S, int D, cons
 template <typename TIn>
 cudaError_t rotate_f16(const void *x, int B, int H, int64_t S, int D, const int64_t st[3],
                        int64_t pos0, __half *out, const AttnArgs &f, cudaStream_t s) {
-  const int64_t n = (int64_t)B * H * S * (D / 8);
+  const int64_t n = (int64_t)B * H * S * rotate_units(D, f.apply_rope, f.rot_dim, f.layout);
   if (n == 0) return cudaSuccess;
   int64_t blocks = (n + 255) / 256;
   const int64_t cap = (int64_t)sm_count_current() * 16;
