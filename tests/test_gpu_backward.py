@@ -97,6 +97,7 @@ TC_CASES = [
     (torch.float16, 1, 4, 4, 130, 200, 64, 70, NEOX, 32),
     (torch.bfloat16, 1, 8, 2, 512, 512, 128, 0, NEOX, 64),
     (torch.bfloat16, 1, 2, 1, 100, 400, 128, 100, GPTJ, 128),  # keys past the last query
+    (torch.float16, 1, 4, 2, 190, 220, 128, 30, GPTJ, 48),     # GPT-J partial: unrotated tail
 ]
 
 
