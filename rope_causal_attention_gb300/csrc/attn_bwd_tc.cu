@@ -100,9 +100,11 @@ template <int D> struct BCfg {
   static constexpr int K_OFF_DO = K_OFF_Q + NS * TILE;
   static constexpr int K_OFF_ST = K_OFF_DO + NS * TILE;
   static constexpr int K_OFF_BAR = K_OFF_ST + NS * 1024;
+  // S^T, dP^T and P^T/dS^T per 64-query half-unit, two TMEM buffers: one
+  // barrier of each per buffer
   static constexpr int KB_KVFULL = 0, KB_QFULL = 1, KB_QEMPTY = 1 + NS, KB_SFULL = 1 + 2 * NS,
-                       KB_DPFULL = 2 + 2 * NS, KB_PFULL = 3 + 2 * NS, KB_ACC = 4 + 2 * NS,
-                       KB_DONE = 5 + 2 * NS, KB_N = 6 + 2 * NS;
+                       KB_DPFULL = 3 + 2 * NS, KB_PFULL = 5 + 2 * NS, KB_ACC = 7 + 2 * NS,
+                       KB_DONE = 8 + 2 * NS, KB_N = 9 + 2 * NS;
   static constexpr int K_OFF_MISC = K_OFF_BAR + KB_N * 8;
   static constexpr int K_SMEM = K_OFF_MISC + 16 + 1024;
   // dq kernel: Q~ | dO | K~ ring (NSK) | V ring (NSV)
@@ -331,9 +333,11 @@ __global__ void __launch_bounds__(kThreadsK, 1)
       mbar_init(bar(C::KB_QFULL + i), 33);  // TMA arrive + 32 lanes of row statistics
       mbar_init(bar(C::KB_QEMPTY + i), 1);
     }
-    mbar_init(bar(C::KB_SFULL), 1);
-    mbar_init(bar(C::KB_DPFULL), 1);
-    mbar_init(bar(C::KB_PFULL), 512);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(C::KB_SFULL + i), 1);
+      mbar_init(bar(C::KB_DPFULL + i), 1);
+      mbar_init(bar(C::KB_PFULL + i), 512);
+    }
     mbar_init(bar(C::KB_ACC), 1);
     mbar_init(bar(C::KB_DONE), 1);
     *abort_flag = 0;
@@ -356,34 +360,42 @@ __global__ void __launch_bounds__(kThreadsK, 1)
 
   if (warp < 16) {
     // ========================================================= P^T and dS^T
+    // A unit (q-head, 128-query tile) is processed as two halves of 64
+    // queries; half v uses TMEM buffer v & 1 (S^T at 256 + 128 (v & 1), dP^T
+    // 64 columns further), so the tensor core computes the next half's S^T
+    // and dP^T while the threads turn this half's into P^T and dS^T.
     const int qd = warp & 3, cq = warp >> 2;  // TMEM lane quarter, query-column quarter
     const int t = qd * 32 + lane;  // key row of the tile = TMEM lane
     const uint32_t lanes = tmem + ((uint32_t)(qd * 32) << 16);
     const int64_t j = j0 + t;
     const float sl2 = p.scale_log2;
-    const int c0 = 32 * cq;  // query columns [c0, c0 + 32) of every unit
+    const int c0 = 16 * cq;  // query columns [c0, c0 + 16) of every half
     bool ok = true;
-    for (int u = 0; u < NU; ++u) {
+    for (int v = 0; v < 2 * NU; ++v) {
+      const int u = v >> 1, hh = v & 1, bf = v & 1;
       const int st = u % C::NS;
       const int m = m_first + u % per_g;
-      ok = ok && __all_sync(0xffffffffu, wait_bar(bar(C::KB_QFULL + st), (uint32_t)((u / C::NS) & 1), ctl));
-      ok = ok && __all_sync(0xffffffffu, wait_bar(bar(C::KB_SFULL), (uint32_t)(u & 1), ctl));
+      if (hh == 0)
+        ok = ok && __all_sync(0xffffffffu, wait_bar(bar(C::KB_QFULL + st), (uint32_t)((u / C::NS) & 1), ctl));
+      ok = ok && __all_sync(0xffffffffu, wait_bar(bar(C::KB_SFULL + bf), (uint32_t)((v >> 1) & 1), ctl));
       if (!ok) break;
       tc_fence_after();
       const float4 *lse4 = reinterpret_cast<const float4 *>(smem + C::K_OFF_ST + st * 1024);
       const float4 *dsm4 = lse4 + 32;
-      const int64_t i0 = (int64_t)m * 128;
+      const int q0 = 64 * hh + c0;  // first query row (of the 128-row tile) of this warp
+      const int64_t i0 = (int64_t)m * 128 + 64 * hh;
       const bool straddle = j0 + 127 > p.off + i0;
-      const int64_t lim = j - p.off - i0;  // query column c sees key j iff c >= lim
-      // P^T from S^T first: the exponentials overlap the dP^T products,
-      // which are only waited for before dS^T
-      uint32_t sr[32], dr[32];
-      tmem_ld32(lanes + 256u + (uint32_t)c0, sr);
+      const int64_t lim = j - p.off - i0;  // half column c sees key j iff c >= lim
+      const uint32_t sbuf = lanes + 256u + 128u * (uint32_t)bf;
+      // P^T from S^T first: the exponentials overlap the dP^T product, which
+      // is only waited for before dS^T
+      uint32_t sr[16], dr[16];
+      tmem_ld16(sbuf + (uint32_t)c0, sr);
       {
-        uint32_t pp[16];
+        uint32_t pp[8];
 #pragma unroll
-        for (int e4 = 0; e4 < 8; ++e4) {
-          const float4 l4 = lse4[(c0 >> 2) + e4];
+        for (int e4 = 0; e4 < 4; ++e4) {
+          const float4 l4 = lse4[(q0 >> 2) + e4];
           const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
           for (int k = 0; k < 4; k += 2) {
@@ -399,19 +411,19 @@ __global__ void __launch_bounds__(kThreadsK, 1)
             sr[e + 1] = __float_as_uint(p1);
           }
         }
-        // P^T packed over the first 16 of the S^T columns this warp has read
-        tmem_st16(lanes + 256u + (uint32_t)c0, pp);
+        // P^T packed over the first 8 of the S^T columns this warp has read
+        tmem_st8(sbuf + (uint32_t)c0, pp);
       }
-      if (!__all_sync(0xffffffffu, wait_bar(bar(C::KB_DPFULL), (uint32_t)(u & 1), ctl))) {
+      if (!__all_sync(0xffffffffu, wait_bar(bar(C::KB_DPFULL + bf), (uint32_t)((v >> 1) & 1), ctl))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      tmem_ld32(lanes + 384u + (uint32_t)c0, dr);
-      uint32_t pd[16];
+      tmem_ld16(sbuf + 64u + (uint32_t)c0, dr);
+      uint32_t pd[8];
 #pragma unroll
-      for (int e4 = 0; e4 < 8; ++e4) {
-        const float4 d4 = dsm4[(c0 >> 2) + e4];
+      for (int e4 = 0; e4 < 4; ++e4) {
+        const float4 d4 = dsm4[(q0 >> 2) + e4];
         const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
         for (int k = 0; k < 4; k += 2) {
@@ -420,11 +432,11 @@ __global__ void __launch_bounds__(kThreadsK, 1)
                              __uint_as_float(sr[e + 1]) * (__uint_as_float(dr[e + 1]) - dv[k + 1]));
         }
       }
-      // dS^T packed over the first 16 of the dP^T columns this warp has read
-      tmem_st16(lanes + 384u + (uint32_t)c0, pd);
+      // dS^T packed over the first 8 of the dP^T columns this warp has read
+      tmem_st8(sbuf + 64u + (uint32_t)c0, pd);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(C::KB_PFULL));
+      mbar_arrive(bar(C::KB_PFULL + bf));
     }
     // ---- epilogue: dV straight from TMEM; dK = R(j)^T (scale dK~) through a
     // padded fp32 row per key (the rotation pairs dims across the quarters)
@@ -515,8 +527,8 @@ __global__ void __launch_bounds__(kThreadsK, 1)
   } else {  // MMA issuer: the whole warp, one elected lane issues
     // =================================================================== MMA
     constexpr uint32_t ab = std::is_same<TIn, __nv_bfloat16>::value ? 1u : 0u;
-    constexpr uint32_t IDESC_S = idesc_f16(0u, 0u, 128);   // fp16 K~ x Q~^T
-    constexpr uint32_t IDESC_DP = idesc_f16(ab, 0u, 128);  // V x dO^T
+    constexpr uint32_t IDESC_S = idesc_f16(0u, 0u, 64);    // fp16 K~ x Q~^T, 64 queries
+    constexpr uint32_t IDESC_DP = idesc_f16(ab, 0u, 64);   // V x dO^T, 64 queries
     constexpr uint32_t IDESC_DV = idesc_f16(ab, 1u, D);    // P^T x dO (dO MN-major)
     constexpr uint32_t IDESC_DK = idesc_f16(0u, 1u, D);    // dS^T x Q~ (Q~ MN-major)
     constexpr uint32_t HI = sdesc_hi_sw128(1024);
@@ -527,45 +539,66 @@ __global__ void __launch_bounds__(kThreadsK, 1)
     const uint32_t qmn_lo0 = sdesc_lo(sbase + C::K_OFF_Q, C::SUBT);
     const uint32_t domn_lo0 = sdesc_lo(sbase + C::K_OFF_DO, C::SUBT);
     bool ok = NU == 0 || wait_all(bar(C::KB_KVFULL), 0u, ctl);
-    for (int u = 0; ok && u < NU; ++u) {
-      const int st = u % C::NS;
-      if (!wait_all(bar(C::KB_QFULL + st), (uint32_t)((u / C::NS) & 1), ctl)) {
+    // dV += P^T dO and dK~ += dS^T Q~ of half w (K = 64 queries; query block
+    // kk of 16 is packed over columns [16 kk, 16 kk + 8) of its buffer)
+    auto issue_dvdk = [&](int w) {
+      const int st = (w >> 1) % C::NS, bf = w & 1;
+      const uint32_t so = (uint32_t)((st * C::TILE + (w & 1) * 8192) >> 4);
+      const uint32_t sb = tmem + 256u + 128u * (uint32_t)bf;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_ts_w(tmem, sb + (uint32_t)(16 * kk),
+               sdesc_join(domn_lo0 + so + (uint32_t)(kk * 2048 >> 4), HI), IDESC_DV,
+               (w > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_ts_w(tmem + (uint32_t)D, sb + 64u + (uint32_t)(16 * kk),
+               sdesc_join(qmn_lo0 + so + (uint32_t)(kk * 2048 >> 4), HI), IDESC_DK,
+               (w > 0 || kk > 0) ? 1u : 0u);
+      if (w & 1) tc_commit_w(bar(C::KB_QEMPTY + st));  // both halves of the unit done
+    };
+    // Issue order S^T(v), dP^T(v), dV/dK(v - 1): buffer v & 1 is rewritten
+    // only after the products of half v - 2 that read it.
+    for (int v = 0; ok && v < 2 * NU; ++v) {
+      const int u = v >> 1, st = u % C::NS, bf = v & 1;
+      if ((v & 1) == 0 && !wait_all(bar(C::KB_QFULL + st), (uint32_t)((u / C::NS) & 1), ctl)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t so = (uint32_t)(st * C::TILE >> 4);
+      const uint32_t so = (uint32_t)((st * C::TILE + (v & 1) * 8192) >> 4);
+      const uint32_t sb = tmem + 256u + 128u * (uint32_t)bf;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (uint32_t)(((kk >> 2) * C::SUBT + (kk & 3) * 32) >> 4);
-        mma_ss_w(tmem + 256u, sdesc_join(k_lo + off, HI), sdesc_join(q_lo0 + so + off, HI),
-               IDESC_S, kk > 0 ? 1u : 0u);
+        mma_ss_w(sb, sdesc_join(k_lo + off, HI), sdesc_join(q_lo0 + so + off, HI), IDESC_S,
+               kk > 0 ? 1u : 0u);
       }
-      tc_commit_w(bar(C::KB_SFULL));
+      tc_commit_w(bar(C::KB_SFULL + bf));
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (uint32_t)(((kk >> 2) * C::SUBT + (kk & 3) * 32) >> 4);
-        mma_ss_w(tmem + 384u, sdesc_join(v_lo + off, HI), sdesc_join(do_lo0 + so + off, HI),
+        mma_ss_w(sb + 64u, sdesc_join(v_lo + off, HI), sdesc_join(do_lo0 + so + off, HI),
                IDESC_DP, kk > 0 ? 1u : 0u);
       }
-      tc_commit_w(bar(C::KB_DPFULL));
-      if (!wait_all(bar(C::KB_PFULL), (uint32_t)(u & 1), ctl)) {
-        ok = false;
-        break;
+      tc_commit_w(bar(C::KB_DPFULL + bf));
+      if (v >= 1) {
+        const int w = v - 1;
+        if (!wait_all(bar(C::KB_PFULL + (w & 1)), (uint32_t)((w >> 1) & 1), ctl)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_dvdk(w);
       }
-      tc_fence_after();
-      // 16 queries per step: query block kk is in column quarter kk / 2, 8 packed columns per half
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        mma_ts_w(tmem, tmem + 256u + (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8),
-               sdesc_join(domn_lo0 + so + (uint32_t)(kk * 2048 >> 4), HI), IDESC_DV,
-               (u > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        mma_ts_w(tmem + (uint32_t)D, tmem + 384u + (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8),
-               sdesc_join(qmn_lo0 + so + (uint32_t)(kk * 2048 >> 4), HI), IDESC_DK,
-               (u > 0 || kk > 0) ? 1u : 0u);
-      tc_commit_w(bar(C::KB_QEMPTY + st));
+    }
+    if (ok && NU > 0) {
+      const int w = 2 * NU - 1;
+      ok = wait_all(bar(C::KB_PFULL + (w & 1)), (uint32_t)((w >> 1) & 1), ctl);
+      if (ok) {
+        tc_fence_after();
+        issue_dvdk(w);
+      }
     }
     if (ok && NU > 0) tc_commit_w(bar(C::KB_ACC));
     tc_commit_w(bar(C::KB_DONE));
