@@ -18,14 +18,17 @@
 // kernels, neither using atomics:
 //   bwd_dkdv_tc_kernel: one CTA per (key tile of 128 rows, kv head, batch);
 //     K~ and V stay in shared memory, and the CTA walks every (q-head of the
-//     kv group, query tile) that sees its keys.  Per query tile:
-//       S^T  = K~ Q~^T   (TMEM cols 256..383; M = 128 keys, N = 128 queries)
-//       dP^T = V  dO^T   (TMEM cols 384..511)
+//     kv group, query tile) that sees its keys, in halves of 64 queries.
+//     Half v uses TMEM buffer b = v & 1:
+//       S^T  = K~ Q~^T   (TMEM cols 256 + 128 b ..; M = 128 keys, N = 64 queries)
+//       dP^T = V  dO^T   (the next 64 columns)
 //       threads: P^T (input dtype) over S^T, dS^T (fp16) over dP^T
-//       dV  += P^T  dO   (TS: A = P^T in TMEM, B = dO read MN-major)
+//       dV  += P^T  dO   (TS: A = P^T in TMEM, B = dO read MN-major, K = 64)
 //       dK~ += dS^T Q~   (TS: A = dS^T in TMEM, B = Q~ read MN-major)
-//     dV and dK~ accumulate in TMEM cols 0..2D-1 over the whole walk, so the
-//     group's q-heads are summed inside the CTA.
+//     The MMA order S^T(v), dP^T(v), dV/dK(v-1) overlaps the next half's
+//     products with this half's thread work.  dV and dK~ accumulate in TMEM
+//     cols 0..2D-1 over the whole walk, so the group's q-heads are summed
+//     inside the CTA.
 //   bwd_dq_tc_kernel: one CTA per (query tile, q-head, batch); Q~ and dO stay
 //     in shared memory, key tiles stream.  S alternates between two TMEM
 //     slots (cols 0..127, 128..255), dP has one (256..383) that the threads
@@ -43,9 +46,9 @@
 // for the second, and the TS products address the two halves per k-step);
 // warp 8 issues the TMA loads; warp 9 allocates TMEM and issues the MMAs.
 // dK/dV (576 threads): warps 0-15 compute P^T and dS^T, four warps per lane
-// quadrant, each on a quarter of the 128 query columns (P^T and dS^T packed
-// over the first 16 columns of the warp's own S^T and dP^T columns); warp 16
-// issues the TMA loads and stages the row statistics (one unit ahead);
+// quadrant, each on a quarter of a half's 64 query columns (P^T and dS^T
+// packed over the first 8 columns of the warp's own S^T and dP^T columns);
+// warp 16 issues the TMA loads and stages the row statistics (one unit ahead);
 // warp 17 allocates TMEM and issues the MMAs.  The MMA warps issue
 // warp-wide (one elected lane per instruction).  Every mbarrier wait is
 // bounded (RA_ERR_DEVICE_TIMEOUT, abort flag, drain).
