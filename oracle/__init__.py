@@ -14,7 +14,9 @@ Contents
 * ``decode_attention``: the decoder step's attention over a KV cache of
   already-rotated keys (per sequence, the same naive attention).
 * ``attention_bwd`` (``oracle.backward``): gradients of the fused RoPE
-  attention, probabilities rebuilt from Q and K (numpy, fp64).
+  attention, probabilities rebuilt from Q and K (numpy, fp64);
+  ``attention_bwd_rows``: selected query / key rows of the same gradients,
+  for problems too large to differentiate densely.
 * ``tiled_attention`` (``oracle.tiled``): the Q-block-outer / K-block-inner
   online-softmax recurrence, used only to show that the recurrence reaches
   the naive result.
@@ -221,4 +223,4 @@ def decode_attention(q, k_cache, v_cache, seq_start, kv_len, seq_ids=None,
     return o, lse
 
 
-from .backward import attention_bwd  # noqa: E402,F401
+from .backward import attention_bwd, attention_bwd_rows  # noqa: E402,F401

@@ -121,3 +121,40 @@ def test_invariants(oracle_mod):
                                              kv_offset=off, rot_dim=8, base=30.0)
     assert np.all(dk2[:, :, Sk:] == 0) and np.all(dv2[:, :, Sk:] == 0)
     np.testing.assert_allclose(dq2, dq, atol=1e-12)
+
+
+@pytest.mark.parametrize("layout,rot_dim,off,Hq,Hkv,Sq,Sk", [
+    (NEOX, 16, 0, 4, 2, 9, 9),      # square, full rotation, GQA
+    (GPTJ, 8, 5, 2, 1, 7, 15),      # cached prefix, partial rotation, keys no query sees
+    (NEOX, 12, 3, 6, 3, 11, 14),    # partial NeoX, odd group count
+])
+def test_selected_rows_equal_dense_rows(oracle_mod, layout, rot_dim, off, Hq, Hkv, Sq, Sk):
+    """attention_bwd_rows, asked for every query row and every key row (in a
+    shuffled order), reproduces attention_bwd row by row."""
+    B, D = 2, 16
+    q, k, v, g = inputs(B, Hq, Hkv, Sq, Sk, D, seed=11 + off + Hq)
+    kw = dict(kv_offset=off, rot_dim=rot_dim, base=70.0, layout=layout)
+    dq, dk, dv = oracle_mod.attention_bwd(q, k, v, g, **kw)
+    rng = np.random.default_rng(off)
+    qr = rng.permutation(B * Hq * Sq)
+    kr = rng.permutation(B * Hkv * Sk)
+    sq, sk, sv = oracle_mod.attention_bwd_rows(q, k, v, g, dq_rows=qr, dkv_rows=kr, nthreads=2,
+                                               **kw)
+    np.testing.assert_allclose(sq, dq.reshape(-1, D)[qr], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(sk, dk.reshape(-1, D)[kr], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(sv, dv.reshape(-1, D)[kr], rtol=0, atol=1e-12)
+
+
+def test_selected_rows_no_rope_custom_scale(oracle_mod):
+    B, Hq, Hkv, Sq, Sk, D, off = 1, 4, 1, 6, 10, 8, 4
+    q, k, v, g = inputs(B, Hq, Hkv, Sq, Sk, D, seed=21)
+    kw = dict(kv_offset=off, apply_rope=False, scale=0.35)
+    dq, dk, dv = oracle_mod.attention_bwd(q, k, v, g, **kw)
+    qr, kr = np.array([0, 5, 23, 12]), np.array([9, 0, 4])
+    sq, sk, sv = oracle_mod.attention_bwd_rows(q, k, v, g, dq_rows=qr, dkv_rows=kr, **kw)
+    np.testing.assert_allclose(sq, dq.reshape(-1, D)[qr], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(sk, dk.reshape(-1, D)[kr], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(sv, dv.reshape(-1, D)[kr], rtol=0, atol=1e-12)
+    # only one side asked for: the other comes back as None
+    oq, ok_, ov = oracle_mod.attention_bwd_rows(q, k, v, g, dq_rows=qr[:1], **kw)
+    assert ok_ is None and ov is None and oq.shape == (1, D)
