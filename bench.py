@@ -10,7 +10,11 @@ standalone rope_apply_qk on the continuous-batching workload (bf16, 65536
 tokens of 256 requests, 32 + 8 heads, D=128, in place) and reports its GB/s,
 and the decoder step on the decode workload (512 requests, contexts up to
 131072 keys, ~140 GB of cached bf16 K/V): rope_append_kv plus attn_decode,
-reported as GB/s of the decode attention (object "decode_step").
+reported as GB/s of the decode attention (object "decode_step"); the
+backward of the long-context workload (object "backward"); and the
+configurations small enough to fit in L2, each timed cold (objects "sweep":
+the six bf16 GPT-J shapes with their peak extra memory against |O| + |LSE|,
+"decode_rope": the decode-batch rope_apply_qk, "fp32_attn": the fp32 case).
 
 Timing: W untimed warm-up steps, then K steps, each timed with CUDA events on
 the launching stream; L2 is flushed (a 256 MiB write) before every timed
@@ -495,6 +499,78 @@ def decode_summary(d, hbm_peak, peak_kind):
     return out
 
 
+def cold_ms(call, flush, stream, steps, warmup):
+    """Median device time of one call with L2 flushed before it (CUDA events
+    on the launching stream, the call queued behind a GPU-side sleep)."""
+    for _ in range(warmup):
+        call()
+    ts = []
+    for _ in range(steps):
+        flush_l2(flush)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        call()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+def time_small_configs(ra, args, dev, stream, tf_peak, hbm_peak, peak_kind):
+    """The configurations small enough to fit in L2, each timed cold (L2
+    flushed before every call, median of the timed calls): the bf16 GPT-J
+    sweep (TFLOP/s against the bf16 peak, and the peak device memory one
+    call allocates beyond its inputs against |O| + |LSE|), the decode RoPE
+    batch (GB/s against the HBM copy) and the fp32 attention (device time)."""
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    steps = max(args.steps, 10)
+    sweep = []
+    for W in wl.SWEEP:
+        q, k, v = [t.to(dev) for t in W.inputs()]
+        cos, sin = ra.make_tables(max(W.Sk, W.kv_offset + W.Sq), W.r, W.base, device=dev)
+
+        def call():
+            return ra.attn_fwd_causal_rope(q, k, v, cos, sin, kv_offset=W.kv_offset,
+                                           layout=W.layout)
+        ms = cold_ms(call, flush, stream, steps, args.warmup)
+        torch.cuda.synchronize()
+        base_mem = torch.cuda.memory_allocated()
+        torch.cuda.reset_peak_memory_stats()
+        o, lse = call()
+        torch.cuda.synchronize()
+        extra = torch.cuda.max_memory_allocated() - base_mem
+        o_lse = o.numel() * o.element_size() + lse.numel() * lse.element_size()
+        del o, lse
+        tf = W.flops() / (ms * 1e-3) / 1e12
+        sweep.append({"workload": W.name, "us": ms * 1e3, "TFLOP/s": tf,
+                      "frac": tf / tf_peak, "peak_extra_bytes": int(extra),
+                      "o_plus_lse_bytes": int(o_lse)})
+    R = wl.DECODE_ROPE
+    rq, rk = [t.to(dev) for t in R.inputs()]
+    pos = torch.from_numpy(R.positions()).to(torch.int32).to(dev)
+    cos, sin = ra.make_tables(R.table_rows, R.rot_dim, R.base, device=dev)
+    ms = cold_ms(lambda: ra.rope_apply_qk(rq, rk, pos, cos, sin, layout=R.layout), flush,
+                 stream, steps, args.warmup)
+    gbs = R.algorithmic_bytes() / (ms * 1e-3) / 1e9
+    decode_rope = {"workload": R.name, "us": ms * 1e3, "GB/s": gbs,
+                   "algorithmic_bytes": R.algorithmic_bytes(),
+                   "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak,
+                                "unit": "GB/s", "frac": gbs / hbm_peak,
+                                "peak_kind": f"{peak_kind} HBM copy"},
+                   "l2": "flushed before every call"}
+    F = wl.FP32_ATTN
+    q, k, v = [t.to(dev) for t in F.inputs()]
+    cos, sin = ra.make_tables(max(F.Sk, F.kv_offset + F.Sq), F.r, F.base, device=dev)
+    ms = cold_ms(lambda: ra.attn_fwd_causal_rope(q, k, v, cos, sin, layout=F.layout,
+                                                 softmax_scale=1.0 / 8), flush, stream, steps,
+                 args.warmup)
+    fp32 = {"workload": F.name, "us": ms * 1e3,
+            "GFLOP/s": F.flops() / (ms * 1e-3) / 1e9, "l2": "flushed before every call"}
+    if ra.ra_get_device_status() != 0:
+        raise RuntimeError("device status error in the small configurations")
+    return {"sweep": sweep, "decode_rope": decode_rope, "fp32_attn": fp32}
+
+
 def warm_ms(call, stream, n):
     """Device time per call when calls are pipelined: n calls captured in one
     CUDA graph, one replay timed between two events (no host launch gaps, L2
@@ -654,6 +730,7 @@ def run_ours(args, ws, rank, local):
     r = time_rope(ra, args, dev, stream)
     d = time_decode(ra, args, dev, stream)
     bw = time_backward(ra, W, args, dev, stream)
+    small = time_small_configs(ra, args, dev, stream, tf_peak, hbm_peak, peak_kind)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -694,11 +771,14 @@ def run_ours(args, ws, rank, local):
                                   "note": "2.5x the forward's FLOPs (S, dP, dV, dK, dQ); the "
                                           "kernels recompute S and dP once more for dQ"},
                      "l2": "flushed before every timed call"},
+        "sweep": small["sweep"],
+        "decode_rope": small["decode_rope"],
+        "fp32_attn": small["fp32_attn"],
         "cpu_baseline": cpu,
         "e2e": {"value": a["flops"] / a["e2e_s"] / 1e12 * ws, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": a["h2d"], "d2h_bytes_per_step": a["d2h"],
                 "ms_per_step": a["e2e_s"] * 1e3},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps,  # one attention kernel per timed step
         "clocks": a["clocks"],
         "wall_s_timed_region": a["wall"],
     }

@@ -12,11 +12,13 @@
  *   current device and runs asynchronously; entry points return as soon as
  *   the kernels are launched.
  * - Errors are returned as ra_status codes, never thrown.  Every argument
- *   check happens on the host before any CUDA call, so a rejected call has
- *   no side effect.  ra_last_error() gives a readable reason.
- * - Errors found by a kernel while it runs (a position outside the table)
- *   are recorded in a per-device status word that ra_get_device_status()
- *   reads and clears.
+ *   check happens on the host before any launch or device memory access, so
+ *   a rejected call has no side effect.  ra_last_error() gives a readable
+ *   reason.
+ * - Errors found by a kernel while it runs (a position outside the table, a
+ *   value outside the fp16 range of the tensor-core operands) are recorded
+ *   in a per-device status word that ra_get_device_status() reads and
+ *   clears.
  * - Element strides are counted in elements, not bytes; the innermost
  *   (head-dimension) stride is always 1.
  *
@@ -52,7 +54,9 @@ typedef enum {
   RA_ERR_OVERLAP = -4,         /* an output partially overlaps an input               */
   RA_ERR_CUDA = -5,            /* a CUDA runtime call failed (see ra_last_error)      */
   RA_ERR_DEVICE_TIMEOUT = -6,  /* a kernel gave up waiting on an internal barrier     */
-  RA_ERR_POSITION_RANGE = -7   /* a kernel met a position outside [0, table_rows)     */
+  RA_ERR_POSITION_RANGE = -7,  /* a kernel met a position outside [0, table_rows)     */
+  RA_ERR_RANGE = -8            /* a tensor-core operand left the fp16 range (results
+                                  of that call are not valid)                          */
 } ra_status;
 
 typedef enum { RA_NEOX = 0, RA_GPTJ = 1 } ra_layout;
@@ -137,6 +141,18 @@ ra_status rope_apply_qk(void *q, void *k, void *q_out, void *k_out, ra_dtype dt,
  *   the tensor-core kernel (tcgen05): D in {64, 128}; every pointer 16-byte
  *   aligned and every stride a multiple of 8 elements; rotated Q/K enter the
  *   product as fp16, P and V as dt, accumulation fp32.
+ *   fp16 range ([TR] Correctness requirements: precision of the rotated
+ *   values): every rotated Q/K element must round to a finite fp16 value,
+ *   |x| < 65520 (|x| <= 65504 after rounding).  A rotation |x~| <= |lo| + |hi|
+ *   of its pair, so inputs with |x| <= 32752 always fit.  Otherwise the
+ *   kernel records RA_ERR_RANGE in the device status word and O / LSE are
+ *   not valid.  Every query row is checked; a key row is checked in the key
+ *   tiles some query visits (rows that no query can see never enter a
+ *   product).  Scores are exponentiated in fp32, each as one fused
+ *   multiply-add of the score and the running row maximum in log2 units,
+ *   so the exponent carries a rounding of about |m| 2^-24: scores up to
+ *   ~1e4 in magnitude (after softmax_scale) keep the stated accuracy, and
+ *   at ~1e9 and beyond the exponent can overflow and O / LSE become NaN.
  *   kv_offset >= 0 (so every row sees key 0; a negative offset would leave
  *   rows without keys and is rejected), Sk >= 1, Sq >= 0 (0: no launch).
  *   With apply_rope: 2 <= rot_dim <= D, even, and table_rows >=
@@ -184,6 +200,12 @@ size_t attn_bwd_workspace_size(ra_dtype dt, int B, int Hq, int Hkv, int64_t Sq, 
  *   multiples of 8 elements): rotated Q/K and dS enter the products as fp16,
  *   P, V and dO as dt, accumulation fp32.  Outputs may not overlap any input
  *   or each other (RA_ERR_OVERLAP).
+ *   fp16 range: a rotated Q/K element that does not round to a finite fp16
+ *   value, or a dS = P o (dP - D) term beyond it (|dP - D| grows with
+ *   |dO| |V|), makes the call record RA_ERR_RANGE in the device status word
+ *   (checked on the rotated copies and on the dQ~ / dK~ / dV accumulators,
+ *   which a non-finite dS term always reaches); dq, dk, dv are then not
+ *   valid.
  */
 ra_status attn_bwd_causal_rope(const void *q, const void *k, const void *v, const void *o,
                                const float *lse, const void *dout, void *dq, void *dk, void *dv,
@@ -289,18 +311,25 @@ ra_status attn_decode(const void *q, void *o, float *lse, const ra_kv_cache *cac
  * attn_decode_noalloc -- attn_decode with its split workspace in a fixed
  * region of device memory inside the library instead of a caller buffer;
  * the call itself allocates nothing (no cudaMalloc, no library allocator).
- * The pages have no counterpart: this is a deployment variant for callers
- * that must not hand out scratch memory (e.g. inside CUDA-graph capture).
+ * The pages have no counterpart.  It serves callers that cannot hand out
+ * scratch memory: a serving loop whose device memory budget is fixed when
+ * it starts, a host framework that owns every device allocation, or a path
+ * where a cudaMalloc (which may synchronise the device) is not acceptable.
  *   Same arguments, results and errors as attn_decode without the workspace
- *   pair.  The region holds RA_DECODE_STATIC_SCRATCH_BYTES; sizes whose
+ *   pair.  The region holds RA_DECODE_STATIC_SCRATCH_BYTES on every device
+ *   that loads the library, for the life of the process.  Sizes whose
  *   attn_decode_workspace_size exceeds it return RA_ERR_UNSUPPORTED before
- *   any CUDA call.  Nothing in the region has to start at zero: each call
- *   writes every partial result before reading it.
- *   The region is resolved (cudaGetSymbolAddress) on the first call on each
- *   device, so that first call must not be made during a stream capture;
- *   later calls may be captured.  One region per device: calls that may
- *   overlap in time (different streams, or graphs replayed concurrently)
- *   race on it and give wrong results; order them on one stream.
+ *   any launch or device memory access; the split plan, and so whether a
+ *   shape fits, depends on the device's SM count as well as on the sizes.
+ *   Nothing in the region has to start at zero: each call writes every
+ *   partial result it reads, so what an earlier call left there is never
+ *   used.
+ *   The region's device address is looked up (cudaGetSymbolAddress) by the
+ *   first call on each device, with that device current; make that first
+ *   call before any stream capture.  One region per device: calls that may
+ *   overlap in time on the GPU (different streams, or work queued
+ *   concurrently) race on it and give wrong results; order them on one
+ *   stream.
  */
 #define RA_DECODE_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
 ra_status attn_decode_noalloc(const void *q, void *o, float *lse, const ra_kv_cache *cache,

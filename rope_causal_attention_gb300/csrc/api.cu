@@ -21,13 +21,14 @@ __device__ int g_ra_status_word;
 thread_local char g_last_error[512] = "no error";
 thread_local char g_last_launch[256] = "";
 
+constexpr int kMaxDevices = 64;
+
 // Split-KV workspace of attn_decode_noalloc: one region per device, resolved
 // once per device with cudaGetSymbolAddress (no allocation at call time).
 static __device__ __align__(256) unsigned char g_decode_scratch[RA_DECODE_STATIC_SCRATCH_BYTES];
 std::mutex g_scratch_mu;
-void *g_scratch_ptr[64];
+void *g_scratch_ptr[kMaxDevices];
 
-constexpr int kMaxDevices = 64;
 std::mutex g_status_mu;
 int *g_status_ptr[kMaxDevices];
 
@@ -89,7 +90,7 @@ void *decode_scratch_ptr(cudaError_t *err) {
   int dev = 0;
   *err = cudaGetDevice(&dev);
   if (*err != cudaSuccess) return nullptr;
-  if (dev < 0 || dev >= 64) {
+  if (dev < 0 || dev >= kMaxDevices) {
     *err = cudaErrorInvalidDevice;
     return nullptr;
   }
@@ -212,6 +213,7 @@ const char *ra_status_string(ra_status st) {
     case RA_ERR_CUDA: return "RA_ERR_CUDA: CUDA runtime error";
     case RA_ERR_DEVICE_TIMEOUT: return "RA_ERR_DEVICE_TIMEOUT: kernel barrier wait timed out";
     case RA_ERR_POSITION_RANGE: return "RA_ERR_POSITION_RANGE: position outside the cos/sin table";
+    case RA_ERR_RANGE: return "RA_ERR_RANGE: a tensor-core operand is outside the fp16 range";
   }
   return "unknown ra_status";
 }

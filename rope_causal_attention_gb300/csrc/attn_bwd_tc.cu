@@ -25,8 +25,9 @@
 //       threads: P^T (input dtype) over S^T, dS^T (fp16) over dP^T
 //       dV  += P^T  dO   (TS: A = P^T in TMEM, B = dO read MN-major, K = 64)
 //       dK~ += dS^T Q~   (TS: A = dS^T in TMEM, B = Q~ read MN-major)
-//     The MMA order S^T(v), dP^T(v), dV/dK(v-1) overlaps the next half's
-//     products with this half's thread work.  dV and dK~ accumulate in TMEM
+//     Two warps issue the products, one per buffer, so the next half's
+//     S^T and dP^T overlap this half's thread work and one warp's waits are
+//     covered by the other's products.  dV and dK~ accumulate in TMEM
 //     cols 0..2D-1 over the whole walk, so the group's q-heads are summed
 //     inside the CTA.
 //   bwd_dq_tc_kernel: one CTA per (query tile, q-head, batch); Q~ and dO stay
@@ -45,13 +46,14 @@
 // results into columns they have already read: +0 for the first half, +64
 // for the second, and the TS products address the two halves per k-step);
 // warp 8 issues the TMA loads; warp 9 allocates TMEM and issues the MMAs.
-// dK/dV (576 threads): warps 0-15 compute P^T and dS^T, four warps per lane
+// dK/dV (608 threads): warps 0-15 compute P^T and dS^T, four warps per lane
 // quadrant, each on a quarter of a half's 64 query columns (P^T and dS^T
 // packed over the first 8 columns of the warp's own S^T and dP^T columns);
 // warp 16 issues the TMA loads and stages the row statistics (one unit ahead);
-// warp 17 allocates TMEM and issues the MMAs.  The MMA warps issue
-// warp-wide (one elected lane per instruction).  Every mbarrier wait is
-// bounded (RA_ERR_DEVICE_TIMEOUT, abort flag, drain).
+// warp 17 allocates TMEM; warps 17 and 18 issue the MMAs of the even and the
+// odd halves.  The MMA warps issue warp-wide (one elected lane per
+// instruction).  Every mbarrier wait is bounded (RA_ERR_DEVICE_TIMEOUT,
+// abort flag, drain).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -73,8 +75,8 @@ constexpr int kThreads = 320;  // dQ: 8 compute warps, TMA, MMA
 constexpr int kWarpTma = 8, kWarpMma = 9;
 // dK/dV: 16 compute warps (4 per SM sub-partition: each owns 32 of the 128
 // query columns of a unit), then the TMA and MMA warps
-constexpr int kThreadsK = 576;
-constexpr int kWarpTmaK = 16, kWarpMmaK = 17;
+constexpr int kThreadsK = 608;
+constexpr int kWarpTmaK = 16, kWarpMmaK = 17;  // and kWarpMmaK + 1: the second MMA issuer
 constexpr uint32_t kTmemCols = 512;
 constexpr long long kTimeoutCycles = 1LL << 32;  // about two seconds
 constexpr float kLog2e = 1.4426950408889634f;
@@ -107,7 +109,7 @@ template <int D> struct BCfg {
   // barrier of each per buffer
   static constexpr int KB_KVFULL = 0, KB_QFULL = 1, KB_QEMPTY = 1 + NS, KB_SFULL = 1 + 2 * NS,
                        KB_DPFULL = 3 + 2 * NS, KB_PFULL = 5 + 2 * NS, KB_ACC = 7 + 2 * NS,
-                       KB_DONE = 8 + 2 * NS, KB_N = 9 + 2 * NS;
+                       KB_DONE = 8 + 2 * NS, KB_DVDK = 9 + 2 * NS, KB_N = 10 + 2 * NS;
   static constexpr int K_OFF_MISC = K_OFF_BAR + KB_N * 8;
   static constexpr int K_SMEM = K_OFF_MISC + 16 + 1024;
   // dq kernel: Q~ | dO | K~ ring (NSK) | V ring (NSV)
@@ -233,7 +235,8 @@ __device__ __forceinline__ void store_row(const float *row, bool rotate, int64_t
 // without rotation every chunk is a tail chunk.  One thread per item: fp32
 // arithmetic with the fp32 table (float4 loads: the host passes 16-byte
 // aligned tables and whole 8-element units), one rounding to fp16.  The
-// input is read once, with the streaming cache hint.
+// input is read once, with the streaming cache hint.  A value that does not
+// round to a finite fp16 records RA_ERR_RANGE.
 __host__ __device__ inline int rotate_units(int D, int apply_rope, int rot_dim, int layout) {
   if (!apply_rope) return D >> 3;
   return (layout == RA_NEOX ? rot_dim >> 4 : rot_dim >> 3) + ((D - rot_dim) >> 3);
@@ -253,8 +256,10 @@ __global__ void __launch_bounds__(256) bwd_rotate_f16_kernel(const TIn *__restri
                                                              int64_t pos0, __half *__restrict__ out,
                                                              int apply_rope, int rot_dim,
                                                              int layout, const float *cos_t,
-                                                             const float *sin_t, int64_t n) {
+                                                             const float *sin_t, int64_t n,
+                                                             int *status) {
   const int half = rot_dim >> 1;
+  uint32_t bad = 0;
   const int per_row = rotate_units(D, apply_rope, rot_dim, layout);
   const int nr = apply_rope ? (layout == RA_NEOX ? rot_dim >> 4 : rot_dim >> 3) : 0;
   const int tail0 = apply_rope ? rot_dim >> 3 : 0;  // first tail chunk
@@ -269,7 +274,10 @@ __global__ void __launch_bounds__(256) bwd_rotate_f16_kernel(const TIn *__restri
       const int c = tail0 + (u - nr);
       float a[8];
       unpack16<TIn>(__ldcs(reinterpret_cast<const uint4 *>(src + 8 * c)), a);
-      *reinterpret_cast<uint4 *>(dst + 8 * c) = pack16<__half>(a);
+      const uint4 w = pack16<__half>(a);
+      bad |= f16x2_nonfinite(w.x) | f16x2_nonfinite(w.y) | f16x2_nonfinite(w.z) |
+             f16x2_nonfinite(w.w);
+      *reinterpret_cast<uint4 *>(dst + 8 * c) = w;
       continue;
     }
     const float *cr = cos_t + (pos0 + s) * half, *sr = sin_t + (pos0 + s) * half;
@@ -284,8 +292,12 @@ __global__ void __launch_bounds__(256) bwd_rotate_f16_kernel(const TIn *__restri
         a[e] = lo[e] * cs[e] - hi[e] * sn[e];
         bb[e] = hi[e] * cs[e] + lo[e] * sn[e];
       }
-      *reinterpret_cast<uint4 *>(dst + 8 * u) = pack16<__half>(a);
-      *reinterpret_cast<uint4 *>(dst + 8 * u + half) = pack16<__half>(bb);
+      const uint4 wa = pack16<__half>(a), wb = pack16<__half>(bb);
+      bad |= f16x2_nonfinite(wa.x) | f16x2_nonfinite(wa.y) | f16x2_nonfinite(wa.z) |
+             f16x2_nonfinite(wa.w) | f16x2_nonfinite(wb.x) | f16x2_nonfinite(wb.y) |
+             f16x2_nonfinite(wb.z) | f16x2_nonfinite(wb.w);
+      *reinterpret_cast<uint4 *>(dst + 8 * u) = wa;
+      *reinterpret_cast<uint4 *>(dst + 8 * u + half) = wb;
     } else {
       float xv[8], y[8];
       unpack16<TIn>(__ldcs(reinterpret_cast<const uint4 *>(src + 8 * u)), xv);
@@ -297,9 +309,13 @@ __global__ void __launch_bounds__(256) bwd_rotate_f16_kernel(const TIn *__restri
         y[2 * e] = xv[2 * e] * c4[e] - xv[2 * e + 1] * s4[e];
         y[2 * e + 1] = xv[2 * e + 1] * c4[e] + xv[2 * e] * s4[e];
       }
-      *reinterpret_cast<uint4 *>(dst + 8 * u) = pack16<__half>(y);
+      const uint4 w = pack16<__half>(y);
+      bad |= f16x2_nonfinite(w.x) | f16x2_nonfinite(w.y) | f16x2_nonfinite(w.z) |
+             f16x2_nonfinite(w.w);
+      *reinterpret_cast<uint4 *>(dst + 8 * u) = w;
     }
   }
+  record_range_flag(status, bad);
 }
 
 // ===================================================================== dK, dV
@@ -342,7 +358,8 @@ __global__ void __launch_bounds__(kThreadsK, 1)
       mbar_init(bar(C::KB_PFULL + i), 512);
     }
     mbar_init(bar(C::KB_ACC), 1);
-    mbar_init(bar(C::KB_DONE), 1);
+    mbar_init(bar(C::KB_DONE), 2);  // both MMA issuers
+    mbar_init(bar(C::KB_DVDK), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -442,7 +459,9 @@ __global__ void __launch_bounds__(kThreadsK, 1)
       mbar_arrive(bar(C::KB_PFULL + bf));
     }
     // ---- epilogue: dV straight from TMEM; dK = R(j)^T (scale dK~) through a
-    // padded fp32 row per key (the rotation pairs dims across the quarters)
+    // padded fp32 row per key (the rotation pairs dims across the quarters).
+    // A non-finite accumulator value (a dS^T term past the fp16 range reaches
+    // every dK~ dim of its key) records RA_ERR_RANGE.
     const bool acc = ok && NU > 0 &&
                      __all_sync(0xffffffffu, wait_bar(bar(C::KB_ACC), 0u, ctl));
     const bool write = ok && (NU == 0 || acc);
@@ -452,11 +471,15 @@ __global__ void __launch_bounds__(kThreadsK, 1)
     TIn *dkd = static_cast<TIn *>(p.dk) + b * p.sdk0 + hk * p.sdk1 + j * p.sdk2;
     const bool row_ok = j < p.Sk;
     constexpr int QD = D / 4;  // dims per column quarter
+    uint32_t bad = 0;
 #pragma unroll 1
     for (int c = 0; c < QD / 16; ++c) {
       const int col = QD * cq + 16 * c;
       uint32_t r[16];
       if (acc) tmem_ld16(lanes + (uint32_t)col, r);
+      if (acc)
+#pragma unroll
+        for (int e = 0; e < 16; ++e) bad |= (r[e] & 0x7f800000u) == 0x7f800000u;
       if (write && row_ok) {
         uint4 *d4 = reinterpret_cast<uint4 *>(dvd + col);
 #pragma unroll
@@ -469,9 +492,13 @@ __global__ void __launch_bounds__(kThreadsK, 1)
         }
       }
       if (acc) tmem_ld16(lanes + (uint32_t)(D + col), r);
+      if (acc)
+#pragma unroll
+        for (int e = 0; e < 16; ++e) bad |= (r[e] & 0x7f800000u) == 0x7f800000u;
 #pragma unroll
       for (int e = 0; e < 16; ++e) row[col + e] = acc ? __uint_as_float(r[e]) * p.scale : 0.f;
     }
+    record_range_flag(p.status, bad);
     named_bar_sync(1, 512);  // all quarters of every row are in shared memory
     if (write && row_ok) store_row<D, TIn>(row, true, j, dkd, cq * (D / 32), (cq + 1) * (D / 32), p);
   } else if (warp == kWarpTmaK) {
@@ -527,8 +554,19 @@ __global__ void __launch_bounds__(kThreadsK, 1)
         for (int u = max(0, issued - C::NS); u < issued; ++u)
           wait_bar_drain(bar(C::KB_QFULL + u % C::NS), (uint32_t)((u / C::NS) & 1));
     }
-  } else {  // MMA issuer: the whole warp, one elected lane issues
+  } else {  // MMA issuers: two whole warps, one elected lane of each issues
     // =================================================================== MMA
+    // Warp kWarpMmaK issues every product of the even halves (TMEM buffer 0),
+    // warp kWarpMmaK + 1 those of the odd halves (buffer 1).  One issuing
+    // warp alone cannot keep the tensor core busy: its queue holds only a
+    // few products, and its waits and bookkeeping between groups outlast
+    // them; with two, one issues while the other waits.  Each warp keeps
+    // the in-order rule on its own buffer (S^T of half v + 2 after dV/dK of
+    // half v).  The dV/dK accumulations alternate between the warps; each
+    // waits for the previous half's dV/dK to complete first, so they run in
+    // half order (the first one initialises the accumulators, and the
+    // result does not depend on timing).
+    const int hb = warp - kWarpMmaK;  // halves v with v % 2 == hb
     constexpr uint32_t ab = std::is_same<TIn, __nv_bfloat16>::value ? 1u : 0u;
     constexpr uint32_t IDESC_S = idesc_f16(0u, 0u, 64);    // fp16 K~ x Q~^T, 64 queries
     constexpr uint32_t IDESC_DP = idesc_f16(ab, 0u, 64);   // V x dO^T, 64 queries
@@ -541,69 +579,57 @@ __global__ void __launch_bounds__(kThreadsK, 1)
     const uint32_t do_lo0 = sdesc_lo(sbase + C::K_OFF_DO, 16);
     const uint32_t qmn_lo0 = sdesc_lo(sbase + C::K_OFF_Q, C::SUBT);
     const uint32_t domn_lo0 = sdesc_lo(sbase + C::K_OFF_DO, C::SUBT);
+    const uint32_t sb = tmem + 256u + 128u * (uint32_t)hb;  // this warp's S^T | dP^T buffer
     bool ok = NU == 0 || wait_all(bar(C::KB_KVFULL), 0u, ctl);
-    // dV += P^T dO and dK~ += dS^T Q~ of half w (K = 64 queries; query block
-    // kk of 16 is packed over columns [16 kk, 16 kk + 8) of its buffer)
-    auto issue_dvdk = [&](int w) {
-      const int st = (w >> 1) % C::NS, bf = w & 1;
-      const uint32_t so = (uint32_t)((st * C::TILE + (w & 1) * 8192) >> 4);
-      const uint32_t sb = tmem + 256u + 128u * (uint32_t)bf;
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        mma_ts_w(tmem, sb + (uint32_t)(16 * kk),
-               sdesc_join(domn_lo0 + so + (uint32_t)(kk * 2048 >> 4), HI), IDESC_DV,
-               (w > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        mma_ts_w(tmem + (uint32_t)D, sb + 64u + (uint32_t)(16 * kk),
-               sdesc_join(qmn_lo0 + so + (uint32_t)(kk * 2048 >> 4), HI), IDESC_DK,
-               (w > 0 || kk > 0) ? 1u : 0u);
-      if (w & 1) tc_commit_w(bar(C::KB_QEMPTY + st));  // both halves of the unit done
-    };
-    // Issue order S^T(v), dP^T(v), dV/dK(v - 1): buffer v & 1 is rewritten
-    // only after the products of half v - 2 that read it.
-    for (int v = 0; ok && v < 2 * NU; ++v) {
-      const int u = v >> 1, st = u % C::NS, bf = v & 1;
-      if ((v & 1) == 0 && !wait_all(bar(C::KB_QFULL + st), (uint32_t)((u / C::NS) & 1), ctl)) {
+    for (int v = hb; ok && v < 2 * NU; v += 2) {
+      const int u = v >> 1, st = u % C::NS;
+      const uint32_t so = (uint32_t)((st * C::TILE + hb * 8192) >> 4);
+      if (!wait_all(bar(C::KB_QFULL + st), (uint32_t)((u / C::NS) & 1), ctl)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t so = (uint32_t)((st * C::TILE + (v & 1) * 8192) >> 4);
-      const uint32_t sb = tmem + 256u + 128u * (uint32_t)bf;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (uint32_t)(((kk >> 2) * C::SUBT + (kk & 3) * 32) >> 4);
         mma_ss_w(sb, sdesc_join(k_lo + off, HI), sdesc_join(q_lo0 + so + off, HI), IDESC_S,
-               kk > 0 ? 1u : 0u);
+                 kk > 0 ? 1u : 0u);
       }
-      tc_commit_w(bar(C::KB_SFULL + bf));
+      tc_commit_w(bar(C::KB_SFULL + hb));
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (uint32_t)(((kk >> 2) * C::SUBT + (kk & 3) * 32) >> 4);
         mma_ss_w(sb + 64u, sdesc_join(v_lo + off, HI), sdesc_join(do_lo0 + so + off, HI),
-               IDESC_DP, kk > 0 ? 1u : 0u);
+                 IDESC_DP, kk > 0 ? 1u : 0u);
       }
-      tc_commit_w(bar(C::KB_DPFULL + bf));
-      if (v >= 1) {
-        const int w = v - 1;
-        if (!wait_all(bar(C::KB_PFULL + (w & 1)), (uint32_t)((w >> 1) & 1), ctl)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        issue_dvdk(w);
+      tc_commit_w(bar(C::KB_DPFULL + hb));
+      // P^T and dS^T of half v in the buffer, and the previous half's
+      // accumulation complete
+      if (!wait_all(bar(C::KB_PFULL + hb), (uint32_t)((v >> 1) & 1), ctl) ||
+          (v >= 1 && !wait_all(bar(C::KB_DVDK), (uint32_t)((v - 1) & 1), ctl))) {
+        ok = false;
+        break;
       }
+      tc_fence_after();
+      // dV += P^T dO and dK~ += dS^T Q~ (K = 64 queries; query block kk of
+      // 16 is packed over columns [16 kk, 16 kk + 8) of the buffer)
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_ts_w(tmem, sb + (uint32_t)(16 * kk),
+                 sdesc_join(domn_lo0 + so + (uint32_t)(kk * 2048 >> 4), HI), IDESC_DV,
+                 (v > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_ts_w(tmem + (uint32_t)D, sb + 64u + (uint32_t)(16 * kk),
+                 sdesc_join(qmn_lo0 + so + (uint32_t)(kk * 2048 >> 4), HI), IDESC_DK,
+                 (v > 0 || kk > 0) ? 1u : 0u);
+      tc_commit_w(bar(C::KB_DVDK));
+      // the odd half closes its unit: every product that read the ring slot
+      // has completed (its own in issue order, the even half's before its
+      // dV/dK started)
+      if (hb == 1) tc_commit_w(bar(C::KB_QEMPTY + st));
+      if (v == 2 * NU - 1) tc_commit_w(bar(C::KB_ACC));
     }
-    if (ok && NU > 0) {
-      const int w = 2 * NU - 1;
-      ok = wait_all(bar(C::KB_PFULL + (w & 1)), (uint32_t)((w >> 1) & 1), ctl);
-      if (ok) {
-        tc_fence_after();
-        issue_dvdk(w);
-      }
-    }
-    if (ok && NU > 0) tc_commit_w(bar(C::KB_ACC));
     tc_commit_w(bar(C::KB_DONE));
     wait_bar_drain(bar(C::KB_DONE), 0u);
   }
@@ -745,14 +771,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     float *row = reinterpret_cast<float *>(smem + C::Q_OFF_K) + t * (D + 1);
     constexpr int HD = D / 2;
+    uint32_t bad = 0;  // a non-finite dQ~ value: a dS term past the fp16 range
 #pragma unroll 1
     for (int c = 0; c < HD / 32; ++c) {
       const int col = HD * hf + 32 * c;
       uint32_t rr[32];
       if (acc) tmem_ld32(lanes + 384u + (uint32_t)col, rr);
+      if (acc)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) bad |= (rr[e] & 0x7f800000u) == 0x7f800000u;
 #pragma unroll
       for (int e = 0; e < 32; ++e) row[col + e] = acc ? __uint_as_float(rr[e]) * p.scale : 0.f;
     }
+    record_range_flag(p.status, bad);
     named_bar_sync(1, 256);  // both halves of every row are in shared memory
     if (acc && row_ok)
       store_row<D, TIn>(row, true, qpos,
@@ -904,7 +935,7 @@ cudaError_t rotate_f16(const void *x, int B, int H, int64_t S, int D, const int6
   if (blocks > cap) blocks = cap;
   bwd_rotate_f16_kernel<TIn><<<(unsigned)blocks, 256, 0, s>>>(
       static_cast<const TIn *>(x), H, S, D, st[0], st[1], st[2], pos0, out, f.apply_rope,
-      f.rot_dim, f.layout, f.cos_t, f.sin_t, n);
+      f.rot_dim, f.layout, f.cos_t, f.sin_t, n, f.status);
   note_launch("bwd_rotate_f16_kernel");
   return cudaGetLastError();
 }

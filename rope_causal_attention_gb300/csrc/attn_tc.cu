@@ -195,14 +195,18 @@ __device__ __forceinline__ uint32_t f16x2(float lo, float hi) {
 
 // Stores 8 values as fp16 into 16-byte chunk c of row `row` of a 128-row tile
 // laid out as 64-column sub-tiles with the 128-byte swizzle (chunk index XOR
-// row mod 8), the layout the tcgen05 K-major descriptor expects.
-__device__ __forceinline__ void st_chunk(uint8_t *tile, int row, int c, const float *f) {
+// row mod 8), the layout the tcgen05 K-major descriptor expects.  `bad`
+// collects the fp16 overflow flags of the stored values.
+__device__ __forceinline__ void st_chunk(uint8_t *tile, int row, int c, const float *f,
+                                         uint32_t &bad) {
   const int sub = c >> 3, cc = c & 7;
   uint4 u;
   u.x = f16x2(f[0], f[1]);
   u.y = f16x2(f[2], f[3]);
   u.z = f16x2(f[4], f[5]);
   u.w = f16x2(f[6], f[7]);
+  bad |= f16x2_nonfinite(u.x) | f16x2_nonfinite(u.y) | f16x2_nonfinite(u.z) |
+         f16x2_nonfinite(u.w);
   *reinterpret_cast<uint4 *>(tile + sub * 16384 + row * 128 + ((cc ^ (row & 7)) << 4)) = u;
 }
 
@@ -216,12 +220,12 @@ __device__ __forceinline__ void ld_table4(const float *p, float *f) {
 // NeoX pairs (i, i + r/2), GPT-J pairs (2i, 2i+1); dims past rot_dim copied.
 template <int D, typename TIn>
 __device__ __forceinline__ void rotate_row(const TIn *src, bool valid, int64_t pos, uint8_t *tile,
-                                           int row, const TcParams &p) {
+                                           int row, const TcParams &p, uint32_t &bad) {
   constexpr int NC = D / 8;
   if (!valid) {
     const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int c = 0; c < NC; ++c) st_chunk(tile, row, c, z);
+    for (int c = 0; c < NC; ++c) st_chunk(tile, row, c, z, bad);
     return;
   }
   const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
@@ -246,8 +250,8 @@ __device__ __forceinline__ void rotate_row(const TIn *src, bool valid, int64_t p
           a[e] = lo[e] * cs[e] - hi[e] * sn[e];
           b[e] = hi[e] * cs[e] + lo[e] * sn[e];
         }
-        st_chunk(tile, row, c, a);
-        st_chunk(tile, row, c + hc, b);
+        st_chunk(tile, row, c, a, bad);
+        st_chunk(tile, row, c + hc, b, bad);
       }
     } else {
       const int rc = p.rot_dim >> 3;  // chunks of 4 pairs
@@ -262,7 +266,7 @@ __device__ __forceinline__ void rotate_row(const TIn *src, bool valid, int64_t p
           y[2 * e] = x[2 * e] * cs[e] - x[2 * e + 1] * sn[e];
           y[2 * e + 1] = x[2 * e + 1] * cs[e] + x[2 * e] * sn[e];
         }
-        st_chunk(tile, row, c, y);
+        st_chunk(tile, row, c, y, bad);
       }
     }
     done = p.rot_dim >> 3;
@@ -270,7 +274,7 @@ __device__ __forceinline__ void rotate_row(const TIn *src, bool valid, int64_t p
   for (int c = done; c < NC; ++c) {
     float x[8];
     In16<TIn>::unpack(__ldg(s4 + c), x);
-    st_chunk(tile, row, c, x);
+    st_chunk(tile, row, c, x, bad);
   }
 }
 
@@ -347,7 +351,7 @@ __device__ __forceinline__ void full_rot_store(
     const uint4 (&raw)[FullRot<D, LAYOUT>::RPG][FullRot<D, LAYOUT>::LD],
     float2 (&cb)[FullRot<D, LAYOUT>::NG], float2 (&sb)[FullRot<D, LAYOUT>::NG],
     const float2 (&cst)[FullRot<D, LAYOUT>::NG], const float2 (&sst)[FullRot<D, LAYOUT>::NG],
-    uint8_t *tile, int t) {
+    uint8_t *tile, int t, uint32_t &bad) {
   using F = FullRot<D, LAYOUT>;
   const int c = t % F::CH, r0 = (t / F::CH) * F::RPG;
 #pragma unroll
@@ -379,6 +383,11 @@ __device__ __forceinline__ void full_rot_store(
       }
     }
     const int sw = row & 7;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      bad |= f16x2_nonfinite(olo[j]);
+      if (LAYOUT == RA_NEOX) bad |= f16x2_nonfinite(ohi[j]);
+    }
     if (LAYOUT == RA_NEOX) {
       *reinterpret_cast<uint4 *>(tile + (c >> 3) * 16384 + row * 128 + (((c & 7) ^ sw) << 4)) =
           make_uint4(olo[0], olo[1], olo[2], olo[3]);
@@ -404,7 +413,7 @@ __device__ __forceinline__ void full_rot_store(
 template <int D, typename TIn, int LAYOUT>
 __device__ __forceinline__ void rotate_tile_full(const TIn *rows, int64_t row_stride,
                                                  int64_t nvalid, int64_t pos0, uint8_t *tile,
-                                                 int t, const TcParams &p) {
+                                                 int t, const TcParams &p, uint32_t &bad) {
   using F = FullRot<D, LAYOUT>;
   uint4 raw[F::RPG][F::LD];
   float2 cb[F::NG], sb[F::NG], cst[F::NG], sst[F::NG];
@@ -412,7 +421,7 @@ __device__ __forceinline__ void rotate_tile_full(const TIn *rows, int64_t row_st
   full_rot_load<D, TIn, LAYOUT>(rows, row_stride, nvalid, t, raw);
   full_rot_table<D, LAYOUT>(p, r0 < nvalid ? pos0 + r0 : 0, t, cb, sb);
   full_rot_table<D, LAYOUT>(p, p.table_rows > 1 ? 1 : 0, t, cst, sst);
-  full_rot_store<D, TIn, LAYOUT>(raw, cb, sb, cst, sst, tile, t);
+  full_rot_store<D, TIn, LAYOUT>(raw, cb, sb, cst, sst, tile, t, bad);
 }
 
 // A raw K tile staged by TMA (128-byte swizzle, the operand layout) is
@@ -485,6 +494,31 @@ __device__ __forceinline__ void full_rot_inplace(uint8_t *tile, int t,
   }
 }
 
+// fp16 overflow flags of the chunks full_rot_inplace wrote for thread t
+// (read back from shared memory: the same thread wrote them, so no
+// synchronisation is needed, and the rotation loop itself keeps its
+// registers).
+template <int D, int LAYOUT>
+__device__ __forceinline__ uint32_t scan_rotated(const uint8_t *tile, int t) {
+  using F = FullRot<D, LAYOUT>;
+  const int c = t % F::CH, r0 = (t / F::CH) * F::RPG;
+  const int ch = (LAYOUT == RA_NEOX) ? c + D / 16 : c;
+  uint32_t bad = 0;
+#pragma unroll
+  for (int r = 0; r < F::RPG; ++r) {
+    const int row = r0 + r;
+#pragma unroll
+    for (int l = 0; l < F::LD; ++l) {
+      const int k = l ? ch : c;
+      const uint4 w = *reinterpret_cast<const uint4 *>(
+          tile + (k >> 3) * 16384 + row * 128 + (((k & 7) ^ (row & 7)) << 4));
+      bad |= f16x2_nonfinite(w.x) | f16x2_nonfinite(w.y) | f16x2_nonfinite(w.z) |
+             f16x2_nonfinite(w.w);
+    }
+  }
+  return bad;
+}
+
 // Chunk c of row `row` of a swizzled tile.
 __device__ __forceinline__ uint4 *tile_chunk(uint8_t *tile, int row, int c) {
   return reinterpret_cast<uint4 *>(tile + (c >> 3) * 16384 + row * 128 + (((c & 7) ^ (row & 7)) << 4));
@@ -494,7 +528,7 @@ __device__ __forceinline__ uint4 *tile_chunk(uint8_t *tile, int row, int c) {
 // or no rotation): rotated pairs, then the tail converted to fp16.
 template <int D, typename TIn>
 __device__ __forceinline__ void rotate_row_inplace(uint8_t *tile, int row, int64_t pos,
-                                                   const TcParams &p) {
+                                                   const TcParams &p, uint32_t &bad) {
   constexpr int NC = D / 8;
   int done = 0;
   if (p.apply_rope) {
@@ -516,8 +550,8 @@ __device__ __forceinline__ void rotate_row_inplace(uint8_t *tile, int row, int64
           a[e] = lo[e] * cs[e] - hi[e] * sn[e];
           b[e] = hi[e] * cs[e] + lo[e] * sn[e];
         }
-        st_chunk(tile, row, c, a);
-        st_chunk(tile, row, c + hc, b);
+        st_chunk(tile, row, c, a, bad);
+        st_chunk(tile, row, c + hc, b, bad);
       }
     } else {
       for (int c = 0; c < (p.rot_dim >> 3); ++c) {
@@ -530,7 +564,7 @@ __device__ __forceinline__ void rotate_row_inplace(uint8_t *tile, int row, int64
           y[2 * e] = x[2 * e] * cs[e] - x[2 * e + 1] * sn[e];
           y[2 * e + 1] = x[2 * e + 1] * cs[e] + x[2 * e] * sn[e];
         }
-        st_chunk(tile, row, c, y);
+        st_chunk(tile, row, c, y, bad);
       }
     }
     done = p.rot_dim >> 3;
@@ -539,7 +573,7 @@ __device__ __forceinline__ void rotate_row_inplace(uint8_t *tile, int row, int64
     for (int c = done; c < NC; ++c) {
       float x[8];
       In16<TIn>::unpack(*tile_chunk(tile, row, c), x);
-      st_chunk(tile, row, c, x);
+      st_chunk(tile, row, c, x, bad);
     }
   }
 }
@@ -547,14 +581,16 @@ __device__ __forceinline__ void rotate_row_inplace(uint8_t *tile, int row, int64
 // K tiles of the whole key loop: wait for the TMA-staged raw tile, rotate it
 // in place, publish.  The cos/sin of the tile's first rows are loaded one
 // entry ahead, so their latency overlaps the previous tile's wait and
-// rotation instead of stalling the rotation.
+// rotation instead of stalling the rotation.  Tiles from key tile
+// `first_new` on are also checked for fp16 overflow (see the kernel).
 template <int D, typename TIn, int LAYOUT, int NS>
 __device__ __forceinline__ void rotate_k_loop(const TcParams &p, int N, int c0, int c1, int t,
                                               uint8_t *k_tiles, uint32_t kraw0, uint32_t kfull0,
-                                              const Ctl &ctl) {
+                                              int first_new, const Ctl &ctl) {
   using F = FullRot<D, LAYOUT>;
   constexpr int TILE = 128 * D * 2;
   float2 cb[F::NG], sb[F::NG], cn[F::NG], sn[F::NG], cst[F::NG], sst[F::NG];
+  uint32_t bad = 0;
   const int64_t r0 = (t / F::CH) * F::RPG;
   auto row0 = [&](int n) {  // table row of the thread's first row in entry n
     const int64_t j0 = (int64_t)(p.split ? split_tile(n, c0, c1) : n) * 128;
@@ -572,9 +608,12 @@ __device__ __forceinline__ void rotate_k_loop(const TcParams &p, int N, int c0, 
     if (n + 1 < N) full_rot_table<D, LAYOUT>(p, row0(n + 1), t, cn, sn);
     if (!wait_bar(kraw0 + 8u * st, (uint32_t)((n / NS) & 1), ctl)) break;
     full_rot_inplace<D, TIn, LAYOUT>(k_tiles + st * TILE, t, cb, sb, cst, sst);
+    if ((p.split ? split_tile(n, c0, c1) : n) >= first_new)
+      bad |= scan_rotated<D, LAYOUT>(k_tiles + st * TILE, t);
     fence_proxy_async_smem();
     mbar_arrive(kfull0 + 8u * st);
   }
+  record_range_flag(p.status, bad);
 }
 
 __device__ __forceinline__ float max3(float a, float b, float c) {
@@ -693,20 +732,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the rotation warpgroup starts on the K stream
       const TIn *qbase = static_cast<const TIn *>(p.q);
       uint8_t *qtile = smem + C::OFF_Q + slot * C::TILE;
+      uint32_t bad = 0;  // fp16 overflow of a rotated query value
       if (p.apply_rope && p.rot_dim == D) {
         const TIn *rows = qbase + b * p.sq0 + hq * p.sq1 + m0 * p.sq2;
         if (p.layout == RA_NEOX)
-          rotate_tile_full<D, TIn, RA_NEOX>(rows, p.sq2, p.Sq - m0, p.kv_off + m0, qtile, t, p);
+          rotate_tile_full<D, TIn, RA_NEOX>(rows, p.sq2, p.Sq - m0, p.kv_off + m0, qtile, t, p,
+                                            bad);
         else
-          rotate_tile_full<D, TIn, RA_GPTJ>(rows, p.sq2, p.Sq - m0, p.kv_off + m0, qtile, t, p);
+          rotate_tile_full<D, TIn, RA_GPTJ>(rows, p.sq2, p.Sq - m0, p.kv_off + m0, qtile, t, p,
+                                            bad);
       } else {
         const int64_t i = m0 + t;
         const bool valid = i < p.Sq;
         const TIn *src = qbase + b * p.sq0 + hq * p.sq1 + (valid ? i : 0) * p.sq2;
-        rotate_row<D, TIn>(src, valid, p.kv_off + i, qtile, t, p);
+        rotate_row<D, TIn>(src, valid, p.kv_off + i, qtile, t, p, bad);
       }
       fence_proxy_async_smem();
       mbar_arrive(bar(C::B_QFULL + slot));
+      record_range_flag(p.status, bad);
     }
     if (act) {
       const int64_t i = m0 + t;
@@ -844,23 +887,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     // =============================================================== rotation
     setmaxnreg_to<128, kRegRotate>();
     const int t = threadIdx.x - kWarpRot * 32;
+    // fp16 overflow check of the rotated keys.  Every key tile is checked by
+    // the CTA with the lowest query rows that visits it: the CTA whose rows
+    // start at m00 checks the tiles that the rows before m00 (the previous
+    // query tile of the same heads) do not reach, and the first query tile
+    // checks all of its tiles.  The check then costs about one tile per CTA.
+    const int first_new = m00 > 0 ? (int)((m00 - 1 + p.kv_off) / 128) + 1 : 0;
     if (p.apply_rope && p.rot_dim == D) {
       if (p.layout == RA_NEOX)
         rotate_k_loop<D, TIn, RA_NEOX, C::NSK>(p, N, nend0, nend1, t, smem + C::OFF_K,
-                                             bar(C::B_KRAW), bar(C::B_KFULL), ctl);
+                                             bar(C::B_KRAW), bar(C::B_KFULL), first_new, ctl);
       else
         rotate_k_loop<D, TIn, RA_GPTJ, C::NSK>(p, N, nend0, nend1, t, smem + C::OFF_K,
-                                             bar(C::B_KRAW), bar(C::B_KFULL), ctl);
+                                             bar(C::B_KRAW), bar(C::B_KFULL), first_new, ctl);
     } else {
+      uint32_t bad = 0;
       for (int n = 0; n < N; ++n) {
         const int st = n % C::NSK;
         if (!wait_bar(bar(C::B_KRAW + st), (uint32_t)((n / C::NSK) & 1), ctl)) break;
         const int64_t j = (int64_t)ktile(n) * 128 + t;
         if (j < p.Sk)  // rows past Sk were zero-filled by the TMA and stay zero
-          rotate_row_inplace<D, TIn>(smem + C::OFF_K + st * C::TILE, t, j, p);
+          rotate_row_inplace<D, TIn>(smem + C::OFF_K + st * C::TILE, t, j, p, bad);
         fence_proxy_async_smem();
         mbar_arrive(bar(C::B_KFULL + st));
       }
+      record_range_flag(p.status, bad);
     }
   } else {
     setmaxnreg_to<128, kRegCtrl>();

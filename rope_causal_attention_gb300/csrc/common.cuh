@@ -7,10 +7,25 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/rope_attn.h"
+
 namespace ra {
 
 __device__ __forceinline__ void record_status(int *status, int code) {
   if (status) atomicCAS(status, 0, code);
+}
+
+// Nonzero when either fp16 half of w is an infinity or a NaN (exponent field
+// all ones): adding one to a saturated 5-bit exponent carries into the sign
+// position of that half.
+__device__ __forceinline__ uint32_t f16x2_nonfinite(uint32_t w) {
+  return ((w & 0x7c007c00u) + 0x04000400u) & 0x80008000u;
+}
+
+// Records RA_ERR_RANGE once per warp when any lane's flag is set.
+__device__ __forceinline__ void record_range_flag(int *status, uint32_t flag) {
+  if (__any_sync(0xffffffffu, flag != 0u) && (threadIdx.x & 31) == 0)
+    record_status(status, RA_ERR_RANGE);
 }
 
 template <typename T> struct Elem;

@@ -101,11 +101,6 @@ TC_CASES = [
 ]
 
 
-TC_READY = True
-needs_tc = pytest.mark.skipif(not TC_READY, reason="tensor-core backward not built yet")
-
-
-@needs_tc
 @pytest.mark.parametrize("dt,B,Hq,Hkv,Sq,Sk,D,off,layout,rot_dim", TC_CASES)
 def test_tc_backward_matches_oracle(ra, orc, dt, B, Hq, Hkv, Sq, Sk, D, off, layout, rot_dim):
     grads_case(ra, orc, dt, B, Hq, Hkv, Sq, Sk, D, off, layout, rot_dim, seed=Sq + D + off)
@@ -113,10 +108,62 @@ def test_tc_backward_matches_oracle(ra, orc, dt, B, Hq, Hkv, Sq, Sk, D, off, lay
     assert "bwd_dq_tc_kernel" in ra.ra_last_launch()
 
 
-@needs_tc
 def test_tc_backward_no_rope(ra, orc):
     grads_case(ra, orc, torch.bfloat16, 1, 4, 2, 200, 260, 128, 60, NEOX, 128, apply_rope=False,
                seed=8)
+
+
+def test_tc_backward_mid_size_gqa_offset(ra, orc):
+    """Every row of a mid-size case on the long-context paths: four q-heads
+    per kv head, a 512-row cached prefix, base 5e5, NeoX, D = 128, 16 query
+    tiles against 20 key tiles."""
+    grads_case(ra, orc, torch.bfloat16, 1, 8, 2, 2048, 2560, 128, 512, NEOX, 128, seed=77,
+               base=500000.0)
+
+
+def sample_rows(rng, n_all, n, edge):
+    """n seeded random flat rows plus the first and last `edge` rows."""
+    pick = rng.choice(n_all, size=n, replace=False)
+    return np.unique(np.concatenate([pick, np.arange(edge), np.arange(n_all - edge, n_all)]))
+
+
+def test_tc_backward_long_context_workload_sampled(ra, orc):
+    """The long-context GQA workload at full size, called exactly as the
+    benchmark times it (same inputs, dO seeded seed + 7, caller workspace):
+    dq on 1024 seeded query rows plus the first and last 128 of the tensor,
+    dk and dv on 256 seeded key rows of one kv head plus its first and last
+    64, against the selected-rows backward oracle."""
+    W = wl.LONG_GQA
+    dt = wl.DTYPES[W.dtype]
+    q, k, v = W.inputs()
+    g = torch.Generator("cpu").manual_seed(W.seed + 7)
+    dout = wl.randn((W.B, W.Hq, W.Sq, W.D), g, dt)
+    qg, kg, vg, dg = q.cuda(), k.cuda(), v.cuda(), dout.cuda()
+    cos, sin = ra.make_tables(max(W.Sk, W.kv_offset + W.Sq), W.r, W.base)
+    o, lse = ra.attn_fwd_causal_rope(qg, kg, vg, cos, sin, kv_offset=W.kv_offset,
+                                     layout=W.layout)
+    dq, dk, dv = (torch.empty_like(t) for t in (qg, kg, vg))
+    wsb = int(ra.lib().attn_bwd_workspace_size(1, W.B, W.Hq, W.Hkv, W.Sq, W.Sk, W.D))
+    wsp = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    ra.attn_bwd_causal_rope(qg, kg, vg, o, lse, dg, cos, sin, kv_offset=W.kv_offset,
+                            layout=W.layout, dq=dq, dk=dk, dv=dv, workspace=wsp)
+    assert ra.ra_get_device_status() == 0
+    assert "bwd_dkdv_tc_kernel" in ra.ra_last_launch()
+    rng = np.random.default_rng(W.seed)
+    qrows = sample_rows(rng, W.B * W.Hq * W.Sq, 1024, 128)
+    hk = int(rng.integers(0, W.Hkv))
+    krows = hk * W.Sk + sample_rows(rng, W.Sk, 256, 64)
+    ref_dq, ref_dk, ref_dv = orc.attention_bwd_rows(
+        q.float().numpy(), k.float().numpy(), v.float().numpy(), dout.float().numpy(),
+        dq_rows=qrows, dkv_rows=krows, kv_offset=W.kv_offset, base=W.base, layout=W.layout)
+    got = {"dq": dq.float().cpu().numpy().reshape(-1, W.D)[qrows],
+           "dk": dk.float().cpu().numpy().reshape(-1, W.D)[krows],
+           "dv": dv.float().cpu().numpy().reshape(-1, W.D)[krows]}
+    for name, ref in (("dq", ref_dq), ("dk", ref_dk), ("dv", ref_dv)):
+        assert np.isfinite(got[name]).all(), name
+        err = np.abs(got[name].astype(np.float64) - ref).max()
+        bound = TOL[dt] * max(1.0, np.abs(ref).max())
+        assert err <= bound, (name, err, bound)
 
 
 def test_backward_rejections(ra):
