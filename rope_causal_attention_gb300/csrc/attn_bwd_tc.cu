@@ -34,9 +34,9 @@
 //     in shared memory, key tiles stream.  S alternates between two TMEM
 //     slots (cols 0..127, 128..255), dP has one (256..383) that the threads
 //     release as soon as they have read it, dQ~ accumulates in 384..: the
-//     MMA order S(n), dP(n), dQ~ += dS(n-1) K~(n-1) lets the tensor core
-//     compute the next tile's S and dP while the threads turn this tile's
-//     into dS.
+//     two MMA-issuing warps (even and odd key tiles, one S slot each) let
+//     the tensor core compute the next tile's S and dP while the threads
+//     turn this tile's into dS.
 //   The epilogues scale, rotate back with R^T (the table's sine negated) and
 //   store in the input dtype.  A shared-memory tile in the 128-byte swizzled
 //   K-major layout doubles as the MN-major operand of the transposed product,
@@ -45,7 +45,8 @@
 // lane quadrant, each on half of the 128 columns (they pack their 16-bit
 // results into columns they have already read: +0 for the first half, +64
 // for the second, and the TS products address the two halves per k-step);
-// warp 8 issues the TMA loads; warp 9 allocates TMEM and issues the MMAs.
+// warp 8 issues the TMA loads; warp 9 allocates TMEM; warps 9 and 10 issue
+// the MMAs of the even and the odd key tiles.
 // dK/dV (608 threads): warps 0-15 compute P^T and dS^T, four warps per lane
 // quadrant, each on a quarter of a half's 64 query columns (P^T and dS^T
 // packed over the first 8 columns of the warp's own S^T and dP^T columns);
@@ -71,8 +72,8 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 320;  // dQ: 8 compute warps, TMA, MMA
-constexpr int kWarpTma = 8, kWarpMma = 9;
+constexpr int kThreads = 352;  // dQ: 8 compute warps, TMA, two MMA issuers
+constexpr int kWarpTma = 8, kWarpMma = 9;  // and kWarpMma + 1
 // dK/dV: 16 compute warps (4 per SM sub-partition: each owns 32 of the 128
 // query columns of a unit), then the TMA and MMA warps
 constexpr int kThreadsK = 608;
@@ -123,7 +124,7 @@ template <int D> struct BCfg {
                        QB_DPFULL = 3 + 2 * NSK + 2 * NSV, QB_DPFREE = 4 + 2 * NSK + 2 * NSV,
                        QB_PFULL = 5 + 2 * NSK + 2 * NSV,  // two S slots
                        QB_ACC = 7 + 2 * NSK + 2 * NSV, QB_DONE = 8 + 2 * NSK + 2 * NSV,
-                       QB_N = 9 + 2 * NSK + 2 * NSV;
+                       QB_DQ = 9 + 2 * NSK + 2 * NSV, QB_N = 10 + 2 * NSK + 2 * NSV;
   static constexpr int Q_OFF_MISC = Q_OFF_BAR + QB_N * 8;
   static constexpr int Q_SMEM = Q_OFF_MISC + 16 + 1024;
   static_assert(K_SMEM <= 232448 && Q_SMEM <= 232448, "shared memory");
@@ -684,7 +685,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(C::QB_DPFULL), 1);
     mbar_init(bar(C::QB_DPFREE), 256);
     mbar_init(bar(C::QB_ACC), 1);
-    mbar_init(bar(C::QB_DONE), 1);
+    mbar_init(bar(C::QB_DONE), 2);  // both MMA issuers
+    mbar_init(bar(C::QB_DQ), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -834,8 +836,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           wait_bar_drain(bar(C::QB_VFULL + n % C::NSV), (uint32_t)((n / C::NSV) & 1));
       }
     }
-  } else {  // MMA issuer: the whole warp, one elected lane issues
+  } else {  // MMA issuers: two whole warps, one elected lane of each issues
     // =================================================================== MMA
+    // Warp kWarpMma issues the products of the even key tiles (S slot 0),
+    // warp kWarpMma + 1 those of the odd ones (S slot 1), so that one warp's
+    // waits are covered by the other's products.  Each keeps S(n + 2) after
+    // dQ~(n) on its own slot (issue order); the shared dP columns are handed
+    // over by the threads (dP of tile n + 1 only after they have read tile
+    // n's); the dQ~ accumulations run in tile order (each waits for the
+    // previous one to complete, so the first initialises the accumulator and
+    // the result does not depend on timing).
+    const int hb = warp - kWarpMma;  // key tiles n with n % 2 == hb
     constexpr uint32_t ab = std::is_same<TIn, __nv_bfloat16>::value ? 1u : 0u;
     constexpr uint32_t IDESC_S = idesc_f16(0u, 0u, 128);   // fp16 Q~ x K~^T
     constexpr uint32_t IDESC_DP = idesc_f16(ab, 0u, 128);  // dO x V^T
@@ -846,22 +857,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t k_lo0 = sdesc_lo(sbase + C::Q_OFF_K, 16);
     const uint32_t v_lo0 = sdesc_lo(sbase + C::Q_OFF_V, 16);
     const uint32_t kmn_lo0 = sdesc_lo(sbase + C::Q_OFF_K, C::SUBT);
+    const uint32_t s_col = tmem + (uint32_t)(128 * hb);  // this warp's S slot
     bool ok = wait_all(bar(C::QB_QFULL), 0u, ctl);
-    // dQ~ += dS(m) K~(m), A = dS packed in S slot m & 1 (keys 64..127 at +64)
-    auto issue_dq = [&](int mm) {
-      const int st = mm % C::NSK, sl = mm & 1;
-      const uint32_t so = (uint32_t)(st * C::TILE >> 4);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        mma_ts_w(tmem + 384u, tmem + (uint32_t)(128 * sl + (kk >> 2) * 64 + (kk & 3) * 8),
-               sdesc_join(kmn_lo0 + so + (uint32_t)(kk * 2048 >> 4), HI), IDESC_DQ,
-               (mm > 0 || kk > 0) ? 1u : 0u);
-      tc_commit_w(bar(C::QB_KEMPTY + st));
-    };
-    // Issue order S(n), dP(n), dQ~(n-1): the tensor core computes the next
-    // tile's S and dP while the threads turn this tile's into dS.
-    for (int n = 0; ok && n < N; ++n) {
-      const int stk = n % C::NSK, stv = n % C::NSV, sl = n & 1;
+    for (int n = hb; ok && n < N; n += 2) {
+      const int stk = n % C::NSK, stv = n % C::NSV;
       if (!wait_all(bar(C::QB_KFULL + stk), (uint32_t)((n / C::NSK) & 1), ctl)) {
         ok = false;
         break;
@@ -871,10 +870,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (uint32_t)(((kk >> 2) * C::SUBT + (kk & 3) * 32) >> 4);
-        mma_ss_w(tmem + (uint32_t)(128 * sl), sdesc_join(q_lo + off, HI),
-               sdesc_join(k_lo0 + sok + off, HI), IDESC_S, kk > 0 ? 1u : 0u);
+        mma_ss_w(s_col, sdesc_join(q_lo + off, HI), sdesc_join(k_lo0 + sok + off, HI), IDESC_S,
+                 kk > 0 ? 1u : 0u);
       }
-      tc_commit_w(bar(C::QB_SFULL + sl));
+      tc_commit_w(bar(C::QB_SFULL + hb));
       if (!wait_all(bar(C::QB_VFULL + stv), (uint32_t)((n / C::NSV) & 1), ctl) ||
           (n >= 1 && !wait_all(bar(C::QB_DPFREE), (uint32_t)((n - 1) & 1), ctl))) {
         ok = false;
@@ -885,26 +884,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (uint32_t)(((kk >> 2) * C::SUBT + (kk & 3) * 32) >> 4);
         mma_ss_w(tmem + 256u, sdesc_join(do_lo + off, HI), sdesc_join(v_lo0 + sov + off, HI),
-               IDESC_DP, kk > 0 ? 1u : 0u);
+                 IDESC_DP, kk > 0 ? 1u : 0u);
       }
       tc_commit_w(bar(C::QB_DPFULL));
       tc_commit_w(bar(C::QB_VEMPTY + stv));
-      if (n >= 1) {
-        if (!wait_all(bar(C::QB_PFULL + ((n - 1) & 1)), (uint32_t)(((n - 1) >> 1) & 1), ctl)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        issue_dq(n - 1);
+      // dS of tile n in the slot, and the previous tile's dQ~ complete
+      if (!wait_all(bar(C::QB_PFULL + hb), (uint32_t)((n >> 1) & 1), ctl) ||
+          (n >= 1 && !wait_all(bar(C::QB_DQ), (uint32_t)((n - 1) & 1), ctl))) {
+        ok = false;
+        break;
       }
-    }
-    if (ok && N > 0) {
-      ok = wait_all(bar(C::QB_PFULL + ((N - 1) & 1)), (uint32_t)(((N - 1) >> 1) & 1), ctl);
-      if (ok) {
-        tc_fence_after();
-        issue_dq(N - 1);
-        tc_commit_w(bar(C::QB_ACC));
-      }
+      tc_fence_after();
+      // dQ~ += dS(n) K~(n), A = dS packed in the slot (keys 64..127 at +64)
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ts_w(tmem + 384u, s_col + (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8),
+                 sdesc_join(kmn_lo0 + sok + (uint32_t)(kk * 2048 >> 4), HI), IDESC_DQ,
+                 (n > 0 || kk > 0) ? 1u : 0u);
+      tc_commit_w(bar(C::QB_DQ));
+      tc_commit_w(bar(C::QB_KEMPTY + stk));
+      if (n == N - 1) tc_commit_w(bar(C::QB_ACC));
     }
     tc_commit_w(bar(C::QB_DONE));
     wait_bar_drain(bar(C::QB_DONE), 0u);
