@@ -356,7 +356,7 @@ __global__ void __launch_bounds__(kThreadsK, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(C::KB_SFULL + i), 1);
       mbar_init(bar(C::KB_DPFULL + i), 1);
-      mbar_init(bar(C::KB_PFULL + i), 512);
+      mbar_init(bar(C::KB_PFULL + i), 16);  // one arrive per compute warp
     }
     mbar_init(bar(C::KB_ACC), 1);
     mbar_init(bar(C::KB_DONE), 2);  // both MMA issuers
@@ -457,7 +457,8 @@ __global__ void __launch_bounds__(kThreadsK, 1)
       tmem_st8(sbuf + 64u + (uint32_t)c0, pd);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(C::KB_PFULL + bf));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::KB_PFULL + bf));
     }
     // ---- epilogue: dV straight from TMEM; dK = R(j)^T (scale dK~) through a
     // padded fp32 row per key (the rotation pairs dims across the quarters).
@@ -680,10 +681,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(C::QB_SFULL + i), 1);
-      mbar_init(bar(C::QB_PFULL + i), 256);
+      mbar_init(bar(C::QB_PFULL + i), 8);  // one arrive per compute warp
     }
     mbar_init(bar(C::QB_DPFULL), 1);
-    mbar_init(bar(C::QB_DPFREE), 256);
+    mbar_init(bar(C::QB_DPFREE), 8);
     mbar_init(bar(C::QB_ACC), 1);
     mbar_init(bar(C::QB_DONE), 2);  // both MMA issuers
     mbar_init(bar(C::QB_DQ), 1);
@@ -751,7 +752,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t dr[64];
       tmem_ld64(lanes + 256u + (uint32_t)(64 * hf), dr);
       tc_fence_before();
-      mbar_arrive(bar(C::QB_DPFREE));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::QB_DPFREE));
 #pragma unroll
       for (int bt = 0; bt < 2; ++bt) {
         uint32_t pd[16];
@@ -766,7 +768,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(C::QB_PFULL + sl));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::QB_PFULL + sl));
     }
     // ---- epilogue: dq = R(kv_offset + i)^T (scale dQ~) through a padded row
     const bool acc = ok && __all_sync(0xffffffffu, wait_bar(bar(C::QB_ACC), 0u, ctl));
