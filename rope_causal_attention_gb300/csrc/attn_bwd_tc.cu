@@ -41,7 +41,7 @@
 //   store in the input dtype.  A shared-memory tile in the 128-byte swizzled
 //   K-major layout doubles as the MN-major operand of the transposed product,
 //   so each operand tile is loaded once.
-// Roles.  dQ (320 threads): warps 0-7 compute P and dS, two warps per TMEM
+// Roles.  dQ (352 threads): warps 0-7 compute P and dS, two warps per TMEM
 // lane quadrant, each on half of the 128 columns (they pack their 16-bit
 // results into columns they have already read: +0 for the first half, +64
 // for the second, and the TS products address the two halves per k-step);
