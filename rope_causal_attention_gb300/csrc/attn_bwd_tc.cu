@@ -642,6 +642,26 @@ __global__ void __launch_bounds__(kThreadsK, 1)
   if (warp == kWarpMmaK) tmem_dealloc(tmem, kTmemCols);
 }
 
+
+// 2^x for x <= ~0 on the FMA pipe: Cody-Waite split x = j + f (j the nearest
+// integer, found by adding 1.5 * 2^23), 2^f on [-0.5, 0.5] by a degree-3
+// minimax polynomial (relative error below 7.5e-5), 2^j added to the
+// exponent field.  Inputs below -125 are clamped (the result is then a
+// tiny normal number, not 0).
+__device__ __forceinline__ float2 ex2_fma2(float2 x) {
+  x.x = fmaxf(x.x, -125.f);
+  x.y = fmaxf(x.y, -125.f);
+  const float2 y = __fadd2_rn(x, make_float2(12582912.f, 12582912.f));
+  const float2 jf = __fadd2_rn(y, make_float2(-12582912.f, -12582912.f));
+  const float2 f = __ffma2_rn(jf, make_float2(-1.f, -1.f), x);
+  float2 p = __ffma2_rn(make_float2(0.0551716685295105f, 0.0551716685295105f), f,
+                        make_float2(0.2426111251115799f, 0.2426111251115799f));
+  p = __ffma2_rn(p, f, make_float2(0.6932609677314758f, 0.6932609677314758f));
+  p = __ffma2_rn(p, f, make_float2(0.9999280571937561f, 0.9999280571937561f));
+  return make_float2(__int_as_float(__float_as_int(p.x) + (__float_as_int(y.x) << 23)),
+                     __int_as_float(__float_as_int(p.y) + (__float_as_int(y.y) << 23)));
+}
+
 // ========================================================================= dQ
 template <int D, typename TIn>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -736,8 +756,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int x = 0; x < 64; x += 2) {
         const int c = 64 * hf + x;
-        float p0 = ex2(fmaf(__uint_as_float(sr[x]), sl2, -lse2));
-        float p1 = ex2(fmaf(__uint_as_float(sr[x + 1]), sl2, -lse2));
+        const float2 xa = __ffma2_rn(make_float2(__uint_as_float(sr[x]), __uint_as_float(sr[x + 1])),
+                                     make_float2(sl2, sl2), make_float2(-lse2, -lse2));
+        float p0, p1;
+        if (x < 16) {  // a quarter of the exponentials on the FMA pipe
+          const float2 pe = ex2_fma2(xa);
+          p0 = pe.x;
+          p1 = pe.y;
+        } else {
+          p0 = ex2(xa.x);
+          p1 = ex2(xa.y);
+        }
         if (straddle) {
           if (c > lim) p0 = 0.f;
           if (c + 1 > lim) p1 = 0.f;
