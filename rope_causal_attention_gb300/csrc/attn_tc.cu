@@ -43,6 +43,7 @@
 #include <math.h>
 #include <stdlib.h>
 
+#include <algorithm>
 #include <type_traits>
 
 #include "common.cuh"
@@ -61,6 +62,7 @@ constexpr int kWarpTmaV = 14;  // V tiles: its own warp, so K loads run ahead of
 constexpr int kWarpMma = 13;
 constexpr uint32_t kTmemCols = 512;
 constexpr long long kTimeoutCycles = 1LL << 32;  // about two seconds
+constexpr int kBandKv = 4;                       // kv heads per band of the launch order
 
 template <int D>
 struct TcCfg {
@@ -104,6 +106,7 @@ struct TcParams {
   int64_t sq0, sq1, sq2, sk0, sk1, sk2, so0, so1, so2;
   int64_t Sq, Sk, kv_off;
   int Hq, G, n_units, units_per_b, n_qt, pack_heads;
+  int band_units;  // head units per band of the launch order (a band's kv heads stay in L2)
   int split;  // one query tile per block, its key tiles shared out between the two slots
   int apply_rope, rot_dim, layout;
   const float *cos_t, *sin_t;
@@ -652,13 +655,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- work item, heaviest first: (batch, head unit, query tile).  Two
-  // heads of one kv group share a query tile, or one head takes two adjacent
-  // 128-row tiles, or (split) one head's tile has its key tiles shared out
-  // between the two slots.
+  // ---- work item: (batch, head unit, query tile).  Two heads of one kv
+  // group share a query tile, or one head takes two adjacent 128-row tiles,
+  // or (split) one head's tile has its key tiles shared out between the two
+  // slots.  Blocks run band by band (band_units consecutive head units, the
+  // heads of a few kv heads), heaviest query tile first within a band.
   const int bid = blockIdx.x;
-  const int qt = p.n_qt - 1 - bid / p.n_units;
-  const int unit = bid % p.n_units;
+  const int per_band = p.n_qt * p.band_units;
+  const int band = bid / per_band;
+  const int rb = bid - band * per_band;
+  const int ub = min(p.band_units, p.n_units - band * p.band_units);
+  const int qt = p.n_qt - 1 - rb / ub;
+  const int unit = band * p.band_units + rb % ub;
   const int b = unit / p.units_per_b, hu = unit % p.units_per_b;
   const int h0 = p.pack_heads ? 2 * hu : hu;
   const int h1 = p.pack_heads ? 2 * hu + 1 : hu;
@@ -761,6 +769,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_used = kMFloor, l = 0.f;
       bool ok = true;
       for (int n = 0; n < nend; ++n) {
+        // per-lane wait (a vote here costs ~1 % of the kernel): the warp's
+        // lanes poll one barrier word and one abort word in lockstep, so
+        // they leave together and with the same result
         if (!wait_bar(bar(C::B_SFULL + slot), (uint32_t)(n & 1), ctl)) { ok = false; break; }
         tc_fence_after();
         const int64_t j0 = (int64_t)(kb + n) * 128;
@@ -834,9 +845,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           stats[t] = make_float2(m_used, l);
           mbar_arrive(bar(C::B_MERGE));
         }
-      } else if (ok && wait_bar(bar(C::B_OFULL + slot), 0u, ctl) &&
-                 (!(p.split && act1) || (wait_bar(bar(C::B_MERGE), 0u, ctl) &&
-                                         wait_bar(bar(C::B_OFULL + 1), 0u, ctl)))) {
+      } else if (ok && wait_all(bar(C::B_OFULL + slot), 0u, ctl) &&
+                 (!(p.split && act1) || (wait_all(bar(C::B_MERGE), 0u, ctl) &&
+                                         wait_all(bar(C::B_OFULL + 1), 0u, ctl)))) {
         tc_fence_after();
         const bool merge = p.split && act1;
         float mf = m_used, lf = l, a0 = 1.f, a1 = 0.f;
@@ -1150,6 +1161,10 @@ cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t s) {
     p.n_units = a.B * a.Hq;
     p.n_qt = (int)((a.Sq + 127) / 128);
   }
+  // Past one wave, blocks run in bands of four kv heads' units, heaviest
+  // query tile first within each: the K/V of the heads in flight then stay
+  // in L2 instead of every kv head's being streamed at once.
+  p.band_units = p.split ? p.n_units : std::min(p.n_units, kBandKv * (p.pack_heads ? p.G / 2 : p.G));
   p.apply_rope = a.apply_rope; p.rot_dim = a.rot_dim; p.layout = a.layout;
   p.cos_t = a.cos_t; p.sin_t = a.sin_t; p.table_rows = a.table_rows;
   p.scale_log2 = (float)((double)a.scale * 1.4426950408889634);

@@ -124,6 +124,11 @@ TC_CASES = [
     (torch.bfloat16, 2, 32, 8, 600, 600, 128, 0, NEOX, None),
     (torch.float16, 1, 64, 16, 640, 640, 64, 0, GPTJ, None),
     (torch.bfloat16, 1, 20, 20, 2000, 2000, 128, 0, GPTJ, None),
+    # more blocks than SMs, D = 128, four and eight q-heads per kv head:
+    # q-head pairs with ragged tiles, offsets and both layouts
+    (torch.float16, 1, 32, 8, 1200, 1500, 128, 300, GPTJ, None),
+    (torch.bfloat16, 1, 64, 8, 700, 777, 128, 77, NEOX, None),
+    (torch.bfloat16, 3, 16, 4, 900, 900, 128, 0, GPTJ, None),
 ]
 
 
@@ -139,9 +144,11 @@ def test_tensor_core_without_rope(ra, orc, D):
     run_case(ra, orc, torch.bfloat16, 1, 4, 2, 260, 300, D, 40, apply_rope=False, seed=D)
 
 
-def test_tensor_core_strided_token_major(ra, orc):
-    """Q/K/V stored token-major [B, S, H, D] and passed as [B, H, S, D] views."""
-    run_case(ra, orc, torch.bfloat16, 2, 4, 2, 150, 150, 128, 0, strided=True, seed=4)
+@pytest.mark.parametrize("B,Hq,Hkv,S", [(2, 4, 2, 150), (2, 32, 8, 640)])
+def test_tensor_core_strided_token_major(ra, orc, B, Hq, Hkv, S):
+    """Q/K/V stored token-major [B, S, H, D] and passed as [B, H, S, D] views
+    (a split-block grid, and a grid of q-head pairs past one wave)."""
+    run_case(ra, orc, torch.bfloat16, B, Hq, Hkv, S, S, 128, 0, strided=True, seed=4)
 
 
 def test_tensor_core_custom_scale(ra, orc):

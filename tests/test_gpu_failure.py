@@ -26,9 +26,9 @@ import __graft_entry__ as g
 g.build()
 import rope_causal_attention_gb300 as ra
 import workloads as wl
-Sq, Sk = int(sys.argv[2]), int(sys.argv[3])
-q, k, v = [t.cuda() for t in wl.attn_qkv(1, 2, 1, Sq, Sk, 64, torch.bfloat16, 3)]
-cos, sin = ra.make_tables(Sk, 64, 10000.0)
+Sq, Sk, Hq, Hkv, D = (int(a) for a in sys.argv[2:7])
+q, k, v = [t.cuda() for t in wl.attn_qkv(1, Hq, Hkv, Sq, Sk, D, torch.bfloat16, 3)]
+cos, sin = ra.make_tables(Sk, D, 10000.0)
 ra.attn_fwd_causal_rope(q, k, v, cos, sin, kv_offset=Sk - Sq)
 code = ra.ra_get_device_status()
 print("STATUS", code)
@@ -39,13 +39,16 @@ print("AFTER", ra.ra_get_device_status(), bool(torch.isfinite(o.float()).all()))
 """
 
 
-# one query tile (both slots of a block on it), and three tiles of a grid
-# that fits on the SMs (split blocks: the two slots share out the key tiles)
-@pytest.mark.parametrize("Sq,Sk", [(128, 256), (384, 512)])
-def test_withheld_copy_times_out_cleanly(Sq, Sk):
+# one query tile (both slots of a block on it), three tiles of a grid that
+# fits on the SMs (split blocks: the two slots share out the key tiles), and
+# a grid past one wave (32 q / 8 kv heads, D = 128: 160 blocks of q-head
+# pairs, every block running out its own wait)
+@pytest.mark.parametrize("Sq,Sk,Hq,Hkv,D", [(128, 256, 2, 1, 64), (384, 512, 2, 1, 64),
+                                            (1280, 1280, 32, 8, 128)])
+def test_withheld_copy_times_out_cleanly(Sq, Sk, Hq, Hkv, D):
     env = dict(os.environ, RA_TEST_WITHHOLD_V_TILE0="1")
-    r = subprocess.run([sys.executable, "-c", CHILD, ROOT, str(Sq), str(Sk)], env=env,
-                       capture_output=True, text=True, timeout=300)
+    r = subprocess.run([sys.executable, "-c", CHILD, ROOT, str(Sq), str(Sk), str(Hq), str(Hkv),
+                        str(D)], env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = dict(l.split(" ", 1) for l in r.stdout.splitlines() if l.startswith(("STATUS", "AFTER")))
     assert lines["STATUS"].strip() == "-6"          # RA_ERR_DEVICE_TIMEOUT
