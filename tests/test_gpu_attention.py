@@ -129,6 +129,10 @@ TC_CASES = [
     (torch.float16, 1, 32, 8, 1200, 1500, 128, 300, GPTJ, None),
     (torch.bfloat16, 1, 64, 8, 700, 777, 128, 77, NEOX, None),
     (torch.bfloat16, 3, 16, 4, 900, 900, 128, 0, GPTJ, None),
+    # launch order in bands of four kv heads' head units, the last band
+    # ragged: 18 units in bands of 8 (three batches), 10 units in bands of 4
+    (torch.bfloat16, 3, 12, 3, 1200, 1300, 128, 100, NEOX, None),
+    (torch.float16, 2, 10, 5, 2000, 2000, 64, 0, GPTJ, None),
 ]
 
 
