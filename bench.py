@@ -14,7 +14,9 @@ reported as GB/s of the decode attention (object "decode_step"); the
 backward of the long-context workload (object "backward"); and the
 configurations small enough to fit in L2, each timed cold (objects "sweep":
 the six bf16 GPT-J shapes with their peak extra memory against |O| + |LSE|,
-"decode_rope": the decode-batch rope_apply_qk, "fp32_attn": the fp32 case).
+"decode_rope": the decode-batch rope_apply_qk, "fp32_attn": the fp32 case;
+"cold_floor": a one-element PyTorch kernel timed the same way, the part of
+each of those times that any launch pays).
 
 Timing: W untimed warm-up steps, then K steps, each timed with CUDA events on
 the launching stream; L2 is flushed (a 256 MiB write) before every timed
@@ -568,7 +570,13 @@ def time_small_configs(ra, args, dev, stream, tf_peak, hbm_peak, peak_kind):
             "GFLOP/s": F.flops() / (ms * 1e-3) / 1e9, "l2": "flushed before every call"}
     if ra.ra_get_device_status() != 0:
         raise RuntimeError("device status error in the small configurations")
-    return {"sweep": sweep, "decode_rope": decode_rope, "fp32_attn": fp32}
+    # What any single launch costs under this protocol: a one-element
+    # elementwise kernel (PyTorch's, not the library's) timed the same way.
+    one = torch.zeros(1, device=dev)
+    floor = {"us": cold_ms(lambda: one.add_(1.0), flush, stream, steps, args.warmup) * 1e3,
+             "kernel": "one-element torch add_ (not a library kernel)",
+             "l2": "flushed before every call"}
+    return {"sweep": sweep, "decode_rope": decode_rope, "fp32_attn": fp32, "cold_floor": floor}
 
 
 def warm_ms(call, stream, n):
@@ -774,6 +782,7 @@ def run_ours(args, ws, rank, local):
         "sweep": small["sweep"],
         "decode_rope": small["decode_rope"],
         "fp32_attn": small["fp32_attn"],
+        "cold_floor": small["cold_floor"],
         "cpu_baseline": cpu,
         "e2e": {"value": a["flops"] / a["e2e_s"] / 1e12 * ws, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": a["h2d"], "d2h_bytes_per_step": a["d2h"],
