@@ -15,11 +15,14 @@
 // q-heads of one kv group at the same rows (grouped-query attention), or two
 // consecutive 128-row tiles of one head.  Warp roles (512 threads, four
 // warpgroups whose register shares are re-balanced with setmaxnreg):
-//   warps 0-3   softmax for slot 0 (thread = query row = TMEM lane)
-//   warps 4-7   softmax for slot 1
-//   warps 8-11  rotation: Q tiles once, then each K tile as it is staged:
-//               global bf16/fp16 -> fp32 rotation with the fp32 cos/sin table
-//               -> fp16 operand in 128B-swizzled shared memory
+//   warps 0-3   softmax for slot 0 (thread = query row = TMEM lane); first
+//               rotates the slot's Q tile once (global bf16/fp16 -> fp32
+//               rotation with the fp32 cos/sin table -> fp16 operand in
+//               128B-swizzled shared memory)
+//   warps 4-7   the same for slot 1
+//   warps 8-11  rotation of each K tile in place, once the TMA has staged it
+//               raw in its operand stage (cos/sin advanced row to row by
+//               angle addition), then published to the MMA issuer
 //   warp 12     TMA producer for raw K tiles (into their operand stages)
 //   warp 13     tcgen05 MMA issuer; owns the tensor-memory allocation
 //   warp 14     TMA producer for V tiles (raw, never rotated)
@@ -32,6 +35,11 @@
 // slot are never visited (causal tile skipping); the mask is evaluated only
 // on tiles that straddle the diagonal or the end of K.  No rotated tensor
 // ever reaches global memory.
+//
+// Launch order: past one wave, blocks run in bands of four kv heads' head
+// units, heaviest query tile first within a band, so the K/V of the heads in
+// flight stay in L2; grids that fit on the SMs at once give each block one
+// query tile whose key tiles the two slots share out (split blocks).
 //
 // Every mbarrier wait is bounded: on expiry the kernel records
 // RA_ERR_DEVICE_TIMEOUT, raises a block-wide abort flag, drains the copies
