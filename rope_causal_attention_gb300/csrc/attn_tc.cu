@@ -1070,7 +1070,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int n = 0; ok && n < N; ++n) {
           const int st = n % C::NSV, nst = (n + 1) % C::NSK;
           if (!wait_all(bar(C::B_VFULL + st), (uint32_t)((n / C::NSV) & 1), ctl)) { ok = false; break; }
+          // the next rotated K tile is waited for here, before this tile's
+          // PV products, not between PV(0, n) and S(0, n + 1)
           bool k_next = false;
+          if (n + 1 < N && (part(0, n + 1) || part(1, n + 1))) {
+            if (!wait_all(bar(C::B_KFULL + nst), (uint32_t)(((n + 1) / C::NSK) & 1), ctl)) { ok = false; break; }
+            k_next = true;
+          }
           for (int s = 0; s < 2; ++s) {
             if (!part(s, n)) continue;
             if (!wait_all(bar(C::B_PFULL + s), (uint32_t)(n & 1), ctl)) { ok = false; break; }
