@@ -61,6 +61,7 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include <algorithm>
 #include <type_traits>
 
 #include "common.cuh"
@@ -80,6 +81,7 @@ constexpr int kThreadsK = 608;
 constexpr int kWarpTmaK = 16, kWarpMmaK = 17;  // and kWarpMmaK + 1: the second MMA issuer
 constexpr uint32_t kTmemCols = 512;
 constexpr long long kTimeoutCycles = 1LL << 32;  // about two seconds
+constexpr int kBandKv = 4;                       // kv heads per band of the launch orders
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <typename T> struct Pack16;
@@ -139,6 +141,9 @@ struct BwdTcParams {
   int64_t sdq0, sdq1, sdq2, sdk0, sdk1, sdk2, sdv0, sdv1, sdv2;
   int64_t Sq, Sk, off;
   int B, Hq, Hkv, G, n_qt, n_kt;
+  // launch order: (batch, kv head) units per band of the dK/dV grid and
+  // (batch, q-head) units per band of the dQ grid (all units: no bands)
+  int kv_band, q_band;
   int apply_rope, rot_dim, layout;
   const float *cos_t, *sin_t;
   float scale, scale_log2;
@@ -337,10 +342,17 @@ __global__ void __launch_bounds__(kThreadsK, 1)
   const Ctl ctl{abort_flag, p.status};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- work: key tile kt (low tiles, seen by the most queries, first)
-  const int per_kt = p.B * p.Hkv;
-  const int kt = blockIdx.x / per_kt;
-  const int b = (blockIdx.x % per_kt) / p.Hkv, hk = blockIdx.x % p.Hkv;
+  // ---- work: key tile kt (low tiles, seen by the most queries, first),
+  // band by band of (batch, kv head) units so that the Q~ and dO of the
+  // heads in flight stay in L2
+  const int n_u = p.B * p.Hkv;
+  const int per_band = p.n_kt * p.kv_band;
+  const int band = blockIdx.x / per_band;
+  const int rb = blockIdx.x - band * per_band;
+  const int ub = min(p.kv_band, n_u - band * p.kv_band);
+  const int kt = rb / ub;
+  const int unit = band * p.kv_band + rb % ub;
+  const int b = unit / p.Hkv, hk = unit % p.Hkv;
   const int64_t j0 = (int64_t)kt * 128;
   const int64_t mf = j0 - p.off < 0 ? 0 : (j0 - p.off) / 128;  // first query tile that sees it
   const int m_first = (int)min(mf, (int64_t)p.n_qt);
@@ -680,10 +692,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Ctl ctl{abort_flag, p.status};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- work: query tile m (last tiles, which see the most keys, first)
-  const int per_m = p.B * p.Hq;
-  const int m = p.n_qt - 1 - (int)(blockIdx.x / per_m);
-  const int b = (blockIdx.x % per_m) / p.Hq, h = blockIdx.x % p.Hq;
+  // ---- work: query tile m (last tiles, which see the most keys, first),
+  // band by band of (batch, q-head) units so that the K~ and V of the kv
+  // heads in flight stay in L2
+  const int n_u = p.B * p.Hq;
+  const int per_band = p.n_qt * p.q_band;
+  const int band = blockIdx.x / per_band;
+  const int rb = blockIdx.x - band * per_band;
+  const int ub = min(p.q_band, n_u - band * p.q_band);
+  const int m = p.n_qt - 1 - rb / ub;
+  const int unit = band * p.q_band + rb % ub;
+  const int b = unit / p.Hq, h = unit % p.Hq;
   const int hk = h / p.G;
   const int64_t i0 = (int64_t)m * 128;
   const int64_t last_pos = p.off + min(i0 + 127, p.Sq - 1);
@@ -1050,6 +1069,17 @@ cudaError_t launch_attn_bwd_tc(const BwdArgs &a, cudaStream_t s) {
   p.scale = f.scale;
   p.scale_log2 = (float)((double)f.scale * 1.4426950408889634);
   p.status = f.status;
+  {
+    // Past one wave of blocks, both grids run in bands of four kv heads'
+    // work (dK/dV: four (batch, kv head) units; dQ: their q-heads), heaviest
+    // tiles first within a band: the Q~/dO (dK/dV) and K~/V (dQ) of the
+    // heads in flight then stay in L2.  Long-context GQA workload: DRAM per
+    // call 2.87 -> 1.44 GB, time unchanged or better.
+    const int sms = sm_count_current();
+    const int64_t gk = (int64_t)p.n_kt * p.B * p.Hkv, gq = (int64_t)p.n_qt * p.B * p.Hq;
+    p.kv_band = gk > sms ? std::min(p.B * p.Hkv, kBandKv) : p.B * p.Hkv;
+    p.q_band = gq > sms ? std::min(p.B * p.Hq, kBandKv * p.G) : p.B * p.Hq;
+  }
   if (f.D == 64)
     return bf ? launch_typed<64, __nv_bfloat16>(maps, p, s) : launch_typed<64, __half>(maps, p, s);
   return bf ? launch_typed<128, __nv_bfloat16>(maps, p, s) : launch_typed<128, __half>(maps, p, s);

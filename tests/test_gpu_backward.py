@@ -166,6 +166,40 @@ def test_tc_backward_long_context_workload_sampled(ra, orc):
         assert err <= bound, (name, err, bound)
 
 
+def test_tc_backward_ragged_launch_bands_sampled(ra, orc):
+    """Grids past one wave run in bands of four kv heads' work: with five kv
+    heads the dK/dV grid (40 key tiles x 5 kv heads) has bands of 4 + 1 kv
+    heads and the dQ grid (32 query tiles x 10 q-heads) bands of 8 + 2
+    q-heads.  dq on 512 seeded query rows plus the first and last 64, dk/dv
+    on 128 seeded key rows plus the first and last 32 of kv head 0 and of
+    kv head 4 (the ragged band), against the selected-rows oracle."""
+    B, Hq, Hkv, Sq, Sk, D, off, base = 1, 10, 5, 4096, 5120, 128, 1024, 500000.0
+    dt = torch.bfloat16
+    q, k, v = wl.attn_qkv(B, Hq, Hkv, Sq, Sk, D, dt, seed=61)
+    g = torch.Generator("cpu").manual_seed(62)
+    dout = wl.randn((B, Hq, Sq, D), g, dt)
+    qg, kg, vg, dg = q.cuda(), k.cuda(), v.cuda(), dout.cuda()
+    cos, sin = ra.make_tables(Sk, D, base)
+    o, lse = ra.attn_fwd_causal_rope(qg, kg, vg, cos, sin, kv_offset=off)
+    dq, dk, dv = ra.attn_bwd_causal_rope(qg, kg, vg, o, lse, dg, cos, sin, kv_offset=off)
+    assert ra.ra_get_device_status() == 0
+    assert "bwd_dkdv_tc_kernel" in ra.ra_last_launch()
+    rng = np.random.default_rng(63)
+    qrows = sample_rows(rng, B * Hq * Sq, 512, 64)
+    krows = np.concatenate([hk * Sk + sample_rows(rng, Sk, 128, 32) for hk in (0, Hkv - 1)])
+    ref_dq, ref_dk, ref_dv = orc.attention_bwd_rows(
+        q.float().numpy(), k.float().numpy(), v.float().numpy(), dout.float().numpy(),
+        dq_rows=qrows, dkv_rows=krows, kv_offset=off, base=base, layout=NEOX)
+    got = {"dq": dq.float().cpu().numpy().reshape(-1, D)[qrows],
+           "dk": dk.float().cpu().numpy().reshape(-1, D)[krows],
+           "dv": dv.float().cpu().numpy().reshape(-1, D)[krows]}
+    for name, ref in (("dq", ref_dq), ("dk", ref_dk), ("dv", ref_dv)):
+        assert np.isfinite(got[name]).all(), name
+        err = np.abs(got[name].astype(np.float64) - ref).max()
+        bound = TOL[dt] * max(1.0, np.abs(ref).max())
+        assert err <= bound, (name, err, bound)
+
+
 def test_backward_rejections(ra):
     q = torch.zeros((1, 2, 8, 64), dtype=torch.bfloat16, device="cuda")
     lse = torch.zeros((1, 2, 8), dtype=torch.float32, device="cuda")
