@@ -28,6 +28,12 @@ and a device synchronize bracket the timed region; times are the max over
 ranks.  Under torchrun each rank runs an independent replica (the method has
 no exchange step), so scaling is weak.
 
+End to end ("e2e"): the same attention through the public API with every
+step's q, k, v uploaded from pinned host memory and O, LSE read back, two
+buffer sets and two copy streams overlapping the copies with the attention;
+"e2e.link" gives one step's upload and download timed alone, so a step
+that the host link, not the kernel, bounds is visible as such.
+
 --impl reference times the fp64 CPU oracle on the host cores on a bounded
 sample of the same workload (rows of the attention), same metric and unit.
 """
@@ -325,6 +331,28 @@ def time_attention(ra, W, args, dev, stream, ws, local, host_e2e=True):
             raise RuntimeError("device status error during end-to-end steps")
         out["h2d"] = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
         out["d2h"] = outs[0][0].numel() * outs[0][0].element_size() + outs[0][1].numel() * 4
+        # The host link on its own (one step's copies, nothing else running):
+        # when these take longer than the attention, the end-to-end step is
+        # bound by the copies, not by the kernel.
+        qd, kd, vd, od, _ = sets[0]
+
+        def copy_ms(fn, s):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record(s)
+            with torch.cuda.stream(s):
+                fn()
+            b.record(s)
+            torch.cuda.synchronize()
+            return a.elapsed_time(b)
+        h2d_ms = min(copy_ms(lambda: [d.copy_(h, non_blocking=True)
+                                      for d, h in ((qd, qh), (kd, kh), (vd, vh))], up)
+                     for _ in range(3))
+        d2h_ms = min(copy_ms(lambda: outs[0][0].copy_(od, non_blocking=True), down)
+                     for _ in range(3))
+        out["link"] = {"h2d_GBps": out["h2d"] / (h2d_ms * 1e-3) / 1e9, "h2d_ms": h2d_ms,
+                       "d2h_GBps": outs[0][0].numel() * outs[0][0].element_size()
+                       / (d2h_ms * 1e-3) / 1e9, "d2h_ms": d2h_ms}
     return out
 
 
@@ -786,7 +814,7 @@ def run_ours(args, ws, rank, local):
         "cpu_baseline": cpu,
         "e2e": {"value": a["flops"] / a["e2e_s"] / 1e12 * ws, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": a["h2d"], "d2h_bytes_per_step": a["d2h"],
-                "ms_per_step": a["e2e_s"] * 1e3},
+                "ms_per_step": a["e2e_s"] * 1e3, "link": a["link"]},
         "gpu_launches": args.steps,  # one attention kernel per timed step
         "clocks": a["clocks"],
         "wall_s_timed_region": a["wall"],
