@@ -325,11 +325,10 @@ ra_status attn_decode(const void *q, void *o, float *lse, const ra_kv_cache *cac
  *   partial result it reads, so what an earlier call left there is never
  *   used.
  *   The region's device address is looked up (cudaGetSymbolAddress) by the
- *   first call on each device, with that device current; make that first
- *   call before any stream capture.  One region per device: calls that may
- *   overlap in time on the GPU (different streams, or work queued
- *   concurrently) race on it and give wrong results; order them on one
- *   stream.
+ *   first call on each device, with that device current.  One region per
+ *   device: calls that may overlap in time on the GPU (different streams,
+ *   or work queued concurrently) race on it and give wrong results; order
+ *   them on one stream.
  */
 #define RA_DECODE_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
 ra_status attn_decode_noalloc(const void *q, void *o, float *lse, const ra_kv_cache *cache,
