@@ -96,7 +96,8 @@ struct TcCfg {
   static constexpr int B_DONE = B_OFULL + 2;
   static constexpr int B_KRAW = B_DONE + 1;  // raw K tile landed (TMA), per stage
   static constexpr int B_MERGE = B_KRAW + NSK;  // split blocks: slot 1's row statistics stored
-  static constexpr int NBAR = B_MERGE + 1;
+  static constexpr int B_KRECV = B_MERGE + 1;   // per stage: a rotated K tile copied in by the peer
+  static constexpr int NBAR = B_KRECV + NSK;
   // split blocks leave query buffer 1 unused; slot 1's (m, l) per row go there
   static constexpr int OFF_STATS = OFF_Q + TILE;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
@@ -115,6 +116,7 @@ struct TcParams {
   int64_t Sq, Sk, kv_off;
   int Hq, G, n_units, units_per_b, n_qt, pack_heads;
   int band_units;  // head units per band of the launch order (a band's kv heads stay in L2)
+  int kshare;      // clusters of two CTAs share the rotated K tiles (see the kernel)
   int split;  // one query tile per block, its key tiles shared out between the two slots
   int apply_rope, rot_dim, layout;
   const float *cos_t, *sin_t;
@@ -597,7 +599,8 @@ __device__ __forceinline__ void rotate_row_inplace(uint8_t *tile, int row, int64
 template <int D, typename TIn, int LAYOUT, int NS>
 __device__ __forceinline__ void rotate_k_loop(const TcParams &p, int N, int c0, int c1, int t,
                                               uint8_t *k_tiles, uint32_t kraw0, uint32_t kfull0,
-                                              int first_new, const Ctl &ctl) {
+                                              int first_new, const Ctl &ctl, int n0 = 0,
+                                              int step = 1) {
   using F = FullRot<D, LAYOUT>;
   constexpr int TILE = 128 * D * 2;
   float2 cb[F::NG], sb[F::NG], cn[F::NG], sn[F::NG], cst[F::NG], sst[F::NG];
@@ -608,16 +611,19 @@ __device__ __forceinline__ void rotate_k_loop(const TcParams &p, int N, int c0, 
     return r0 < p.Sk - j0 ? j0 + r0 : 0;
   };
   full_rot_table<D, LAYOUT>(p, p.table_rows > 1 ? 1 : 0, t, cst, sst);
-  if (N > 0) full_rot_table<D, LAYOUT>(p, row0(0), t, cn, sn);
-  for (int n = 0; n < N; ++n) {
+  if (n0 < N) full_rot_table<D, LAYOUT>(p, row0(n0), t, cn, sn);
+  // with step 2 (tiles shared by a cluster) this loop's uses of a stage are
+  // every other use of it
+  for (int n = n0; n < N; n += step) {
     const int st = n % NS;
 #pragma unroll
     for (int j = 0; j < F::NG; ++j) {
       cb[j] = cn[j];
       sb[j] = sn[j];
     }
-    if (n + 1 < N) full_rot_table<D, LAYOUT>(p, row0(n + 1), t, cn, sn);
-    if (!wait_bar(kraw0 + 8u * st, (uint32_t)((n / NS) & 1), ctl)) break;
+    if (n + step < N) full_rot_table<D, LAYOUT>(p, row0(n + step), t, cn, sn);
+    const int use = n / NS;
+    if (!wait_bar(kraw0 + 8u * st, (uint32_t)((step == 2 ? use >> 1 : use) & 1), ctl)) break;
     full_rot_inplace<D, TIn, LAYOUT>(k_tiles + st * TILE, t, cb, sb, cst, sst);
     if ((p.split ? split_tile(n, c0, c1) : n) >= first_new)
       bad |= scan_rotated<D, LAYOUT>(k_tiles + st * TILE, t);
@@ -693,6 +699,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool q1 = act1 && !p.split;  // slot 1 has a query tile of its own
   const int N = p.split ? nq0 : max(nend0, nend1);  // K/V stream entries
   auto ktile = [&](int e) { return p.split ? split_tile(e, nend0, nend1) : e; };
+  // K tiles shared by a cluster of two CTAs (the two head pairs of one kv
+  // head at one query tile, so both visit the same key tiles): CTA rank r
+  // loads and rotates the tiles n with n % 2 == r and copies each, rotated,
+  // into the same stage of the peer.  Each CTA then rotates half of the
+  // tiles it consumes.  A stage's uses alternate between owned and received
+  // tiles (three stages), so each kind's barrier phase advances every other
+  // use.
+  static_assert(C::NSK % 2 == 1, "owned and received uses of a stage alternate only with an odd stage count");
+  const bool kshare = p.kshare != 0;
+  const uint32_t rank = kshare ? cluster_ctarank() : 0u;
+  auto owns = [&](int n) { return !kshare || (n & 1) == (int)rank; };
+  auto kpar = [&](int n) {
+    const int u = n / C::NSK;
+    return (uint32_t)((kshare ? (u >> 1) : u) & 1);
+  };
 
   // ---- set-up: barriers, tensor memory
   if (threadIdx.x == 0) {
@@ -701,7 +722,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < C::NSK; ++i) {
       mbar_init(bar(C::B_KRAW + i), 1);
       mbar_init(bar(C::B_KFULL + i), 128);
-      mbar_init(bar(C::B_KEMPTY + i), 1);
+      mbar_init(bar(C::B_KEMPTY + i), kshare ? 2 : 1);  // released by both CTAs when shared
+      mbar_init(bar(C::B_KRECV + i), 1);
     }
     for (int i = 0; i < C::NSV; ++i) {
       mbar_init(bar(C::B_VFULL + i), 1);
@@ -725,7 +747,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpTma && lane == 0) prefetch_tmap(&tmap_k);
   if (warp == kWarpTmaV && lane == 0) prefetch_tmap(&tmap_v);
   tc_fence_before();
-  __syncthreads();
+  if (kshare)
+    cluster_sync();  // the peer's barriers are initialised before any copy targets them
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -913,12 +938,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // checks all of its tiles.  The check then costs about one tile per CTA.
     const int first_new = m00 > 0 ? (int)((m00 - 1 + p.kv_off) / 128) + 1 : 0;
     if (p.apply_rope && p.rot_dim == D) {
+      // the owned tiles only when a cluster shares them
+      const int n0 = kshare ? (int)rank : 0, step = kshare ? 2 : 1;
       if (p.layout == RA_NEOX)
         rotate_k_loop<D, TIn, RA_NEOX, C::NSK>(p, N, nend0, nend1, t, smem + C::OFF_K,
-                                             bar(C::B_KRAW), bar(C::B_KFULL), first_new, ctl);
+                                             bar(C::B_KRAW), bar(C::B_KFULL), first_new, ctl,
+                                             n0, step);
       else
         rotate_k_loop<D, TIn, RA_GPTJ, C::NSK>(p, N, nend0, nend1, t, smem + C::OFF_K,
-                                             bar(C::B_KRAW), bar(C::B_KFULL), first_new, ctl);
+                                             bar(C::B_KRAW), bar(C::B_KFULL), first_new, ctl,
+                                             n0, step);
     } else {
       uint32_t bad = 0;
       for (int n = 0; n < N; ++n) {
@@ -940,10 +969,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         int k_issued = 0;
         for (int n = 0; n < N; ++n) {
           const int st = n % C::NSK;
-          // raw K tile n into its operand stage, once S(n - NSK) has read the old one
+          // raw K tile n into its operand stage, once S(n - NSK) has read the
+          // old one (in both CTAs when they share K tiles)
           if (n >= C::NSK &&
               !wait_bar(bar(C::B_KEMPTY + st), (uint32_t)((n / C::NSK - 1) & 1), ctl))
             break;
+          k_issued = n + 1;
+          if (!owns(n)) {
+            // the peer copies its rotated tile n into this stage
+            mbar_arrive_expect_tx(bar(C::B_KRECV + st), (uint32_t)C::TILE);
+            continue;
+          }
           const int kt = ktile(n);
           mbar_arrive_expect_tx(bar(C::B_KRAW + st), (uint32_t)C::TILE);
           const int c1 = p.kperm[0] == 0 ? kt * 128 : (p.kperm[0] == 1 ? hk : b);
@@ -953,11 +989,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int sub = 0; sub < D / 64; ++sub)
             tma_load_4d(sbase + C::OFF_K + st * C::TILE + sub * C::SUBT, &tmap_k,
                         bar(C::B_KRAW + st), sub * 64, c1, c2, c3);
-          k_issued = n + 1;
         }
         if (*abort_flag)  // let copies already in flight land before the block exits
           for (int n = max(0, k_issued - C::NSK); n < k_issued; ++n)
-            wait_bar_drain(bar(C::B_KRAW + n % C::NSK), (uint32_t)((n / C::NSK) & 1));
+            wait_bar_drain(bar((owns(n) ? C::B_KRAW : C::B_KRECV) + n % C::NSK), kpar(n));
+      } else if (lane == 1 && kshare) {
+        // each owned tile, once rotated, into the peer's stage (the peer's
+        // stage is free: this CTA's producer waited for both CTAs' release
+        // of it before loading the raw tile)
+        const uint32_t peer = rank ^ 1u;
+        for (int n = (int)rank; n < N; n += 2) {
+          const int st = n % C::NSK;
+          if (!wait_bar(bar(C::B_KFULL + st), kpar(n), ctl)) break;
+          const uint32_t src = sbase + C::OFF_K + st * C::TILE;
+          bulk_copy_to_peer(mapa_rank(src, peer), src, (uint32_t)C::TILE,
+                            mapa_rank(bar(C::B_KRECV + st), peer));
+          bulk_commit_group();
+        }
+        bulk_wait_read_all();  // sources read before this CTA goes on or exits
       }
     } else if (warp == kWarpTmaV) {
       // ================================================================ TMA V
@@ -1056,16 +1105,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
+        // rotated K tile n ready: rotated here, or copied in by the peer
+        auto k_ready = [&](int n) {
+          return wait_all(bar((owns(n) ? C::B_KFULL : C::B_KRECV) + n % C::NSK), kpar(n), ctl);
+        };
+        // a K stage released: by this CTA, and (shared tiles) to the peer too
+        auto k_release = [&](int stage) {
+          if (kshare)
+            tc_commit_mc_w(bar(C::B_KEMPTY + stage), (uint16_t)3);
+          else
+            tc_commit_w(bar(C::B_KEMPTY + stage));
+        };
         if (act0) ok = wait_all(bar(C::B_QFULL + 0), 0u, ctl);
         if (ok && act1) ok = wait_all(bar(C::B_QFULL + 1), 0u, ctl);
-        if (ok && N > 0) ok = wait_all(bar(C::B_KFULL + 0), 0u, ctl);
+        if (ok && N > 0) ok = k_ready(0);
         if (ok && N > 0) {
           for (int s = 0; s < 2; ++s)
             if (part(s, 0)) {
               mma_s(s, 0);
               tc_commit_w(bar(C::B_SFULL + s));
             }
-          tc_commit_w(bar(C::B_KEMPTY + 0));
+          k_release(0);
         }
         for (int n = 0; ok && n < N; ++n) {
           const int st = n % C::NSV, nst = (n + 1) % C::NSK;
@@ -1074,7 +1134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // PV products, not between PV(0, n) and S(0, n + 1)
           bool k_next = false;
           if (n + 1 < N && (part(0, n + 1) || part(1, n + 1))) {
-            if (!wait_all(bar(C::B_KFULL + nst), (uint32_t)(((n + 1) / C::NSK) & 1), ctl)) { ok = false; break; }
+            if (!k_ready(n + 1)) { ok = false; break; }
             k_next = true;
           }
           for (int s = 0; s < 2; ++s) {
@@ -1085,7 +1145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (n == (s ? nend1 : nend0) - 1) tc_commit_w(bar(C::B_OFULL + s));
             if (part(s, n + 1)) {
               if (!k_next) {
-                if (!wait_all(bar(C::B_KFULL + nst), (uint32_t)(((n + 1) / C::NSK) & 1), ctl)) {
+                if (!k_ready(n + 1)) {
                   ok = false;
                   break;
                 }
@@ -1097,7 +1157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!ok) break;
           tc_commit_w(bar(C::B_VEMPTY + st));
-          if (k_next) tc_commit_w(bar(C::B_KEMPTY + nst));
+          if (k_next) k_release(nst);
         }
       }
       // all issued MMAs complete before tensor memory is released
@@ -1108,7 +1168,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  if (kshare)
+    cluster_sync();  // no CTA leaves while its peer may still copy into it
+  else
+    __syncthreads();
   tc_fence_after();
   if (warp == kWarpMma) tmem_dealloc(tmem, kTmemCols);
 }
@@ -1138,8 +1201,25 @@ cudaError_t launch_typed(const AttnArgs &a, const CUtensorMap &kmap, const CUten
     return e;
   });
   if (attr_err != cudaSuccess) return attr_err;
-  attn_tc_kernel<D, TIn><<<grid, kThreads, C::SMEM, s>>>(kmap, vmap, p);
-  return cudaGetLastError();
+  if (!p.kshare) {
+    attn_tc_kernel<D, TIn><<<grid, kThreads, C::SMEM, s>>>(kmap, vmap, p);
+    return cudaGetLastError();
+  }
+  // clusters of two consecutive blocks: the two head pairs of one kv head
+  // at one query tile (see the launch order)
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_tc_kernel<D, TIn>, kmap, vmap, p);
 }
 
 }  // namespace
@@ -1179,6 +1259,14 @@ cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t s) {
   // query tile first within each: the K/V of the heads in flight then stay
   // in L2 instead of every kv head's being streamed at once.
   p.band_units = p.split ? p.n_units : std::min(p.n_units, kBandKv * (p.pack_heads ? p.G / 2 : p.G));
+  // Shared K tiles (clusters of two): D = 128 with full rotation, head pairs
+  // past one wave, and an even number of head pairs per kv head, so that the
+  // launch order puts the two head pairs of one kv head at one query tile in
+  // consecutive blocks (bands and units per band are then even too).
+  p.kshare = (a.D == 128 && !p.split && p.pack_heads && a.apply_rope && a.rot_dim == 128 &&
+              (p.G / 2) % 2 == 0 && p.band_units % 2 == 0 && p.n_units % 2 == 0)
+                 ? 1
+                 : 0;
   p.apply_rope = a.apply_rope; p.rot_dim = a.rot_dim; p.layout = a.layout;
   p.cos_t = a.cos_t; p.sin_t = a.sin_t; p.table_rows = a.table_rows;
   p.scale_log2 = (float)((double)a.scale * 1.4426950408889634);
