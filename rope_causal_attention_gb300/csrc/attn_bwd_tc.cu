@@ -433,8 +433,10 @@ __global__ void __launch_bounds__(kThreadsK, 1)
 #pragma unroll
           for (int k = 0; k < 4; k += 2) {
             const int e = 4 * e4 + k;
-            float p0 = ex2(fmaf(__uint_as_float(sr[e]), sl2, -lv[k]));
-            float p1 = ex2(fmaf(__uint_as_float(sr[e + 1]), sl2, -lv[k + 1]));
+            const float2 xa = __ffma2_rn(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
+                                         make_float2(sl2, sl2), make_float2(-lv[k], -lv[k + 1]));
+            float p0 = ex2(xa.x);
+            float p1 = ex2(xa.y);
             if (straddle) {
               if (c0 + e < lim) p0 = 0.f;
               if (c0 + e + 1 < lim) p1 = 0.f;
@@ -461,8 +463,11 @@ __global__ void __launch_bounds__(kThreadsK, 1)
 #pragma unroll
         for (int k = 0; k < 4; k += 2) {
           const int e = 4 * e4 + k;
-          pd[e >> 1] = f16x2(__uint_as_float(sr[e]) * (__uint_as_float(dr[e]) - dv[k]),
-                             __uint_as_float(sr[e + 1]) * (__uint_as_float(dr[e + 1]) - dv[k + 1]));
+          const float2 ds = __fmul2_rn(
+              make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
+              __fadd2_rn(make_float2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])),
+                         make_float2(-dv[k], -dv[k + 1])));
+          pd[e >> 1] = f16x2(ds.x, ds.y);
         }
       }
       // dS^T packed over the first 8 of the dP^T columns this warp has read
@@ -778,7 +783,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float2 xa = __ffma2_rn(make_float2(__uint_as_float(sr[x]), __uint_as_float(sr[x + 1])),
                                      make_float2(sl2, sl2), make_float2(-lse2, -lse2));
         float p0, p1;
-        if (x < 16) {  // a quarter of the exponentials on the FMA pipe
+        if (x < 8) {  // an eighth of the exponentials on the FMA pipe
           const float2 pe = ex2_fma2(xa);
           p0 = pe.x;
           p1 = pe.y;
@@ -808,8 +813,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const int x = 32 * bt + e;
-          pd[e >> 1] = f16x2(__uint_as_float(sr[x]) * (__uint_as_float(dr[x]) - dsum),
-                             __uint_as_float(sr[x + 1]) * (__uint_as_float(dr[x + 1]) - dsum));
+          const float2 ds = __fmul2_rn(
+              make_float2(__uint_as_float(sr[x]), __uint_as_float(sr[x + 1])),
+              __fadd2_rn(make_float2(__uint_as_float(dr[x]), __uint_as_float(dr[x + 1])),
+                         make_float2(-dsum, -dsum)));
+          pd[e >> 1] = f16x2(ds.x, ds.y);
         }
         // packed into columns this warp has already read: [64 hf + 16 bt, +16)
         tmem_st16(sbase_t + (uint32_t)(64 * hf + 16 * bt), pd);
