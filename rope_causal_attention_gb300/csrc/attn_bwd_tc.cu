@@ -47,12 +47,14 @@
 // for the second, and the TS products address the two halves per k-step);
 // warp 8 issues the TMA loads; warp 9 allocates TMEM; warps 9 and 10 issue
 // the MMAs of the even and the odd key tiles.
-// dK/dV (608 threads): warps 0-15 compute P^T and dS^T, four warps per lane
-// quadrant, each on a quarter of a half's 64 query columns (P^T and dS^T
-// packed over the first 8 columns of the warp's own S^T and dP^T columns);
-// warp 16 issues the TMA loads and stages the row statistics (one unit ahead);
-// warp 17 allocates TMEM; warps 17 and 18 issue the MMAs of the even and the
-// odd halves.  The MMA warps issue warp-wide (one elected lane per
+// dK/dV (352 threads): warps 0-7 compute P^T and dS^T, two warps per lane
+// quadrant, each on 32 of a half's 64 query columns, i.e. two 16-query
+// k-blocks (each block's P^T and dS^T packed over the first 8 of its own 16
+// S^T and dP^T columns); warp 8 issues the TMA loads and stages the row
+// statistics (one unit ahead); warp 9 allocates TMEM; warps 9 and 10 issue
+// the MMAs of the even and the odd halves.  (With 16 compute warps on 16
+// columns each the kernel was ~2 % slower: the issuers then shared their
+// sub-partitions with four busy warps instead of two.)  The MMA warps issue warp-wide (one elected lane per
 // instruction).  Every mbarrier wait is bounded (RA_ERR_DEVICE_TIMEOUT,
 // abort flag, drain).
 #include <cuda.h>
@@ -75,10 +77,10 @@ using namespace ptx;
 
 constexpr int kThreads = 352;  // dQ: 8 compute warps, TMA, two MMA issuers
 constexpr int kWarpTma = 8, kWarpMma = 9;  // and kWarpMma + 1
-// dK/dV: 16 compute warps (4 per SM sub-partition: each owns 32 of the 128
-// query columns of a unit), then the TMA and MMA warps
-constexpr int kThreadsK = 608;
-constexpr int kWarpTmaK = 16, kWarpMmaK = 17;  // and kWarpMmaK + 1: the second MMA issuer
+// dK/dV: 8 compute warps (2 per SM sub-partition: each owns 32 of a half's
+// 64 query columns), then the TMA and MMA warps
+constexpr int kThreadsK = 352;
+constexpr int kWarpTmaK = 8, kWarpMmaK = 9;  // and kWarpMmaK + 1: the second MMA issuer
 constexpr uint32_t kTmemCols = 512;
 constexpr long long kTimeoutCycles = 1LL << 32;  // about two seconds
 constexpr int kBandKv = 4;                       // kv heads per band of the launch orders
@@ -368,7 +370,7 @@ __global__ void __launch_bounds__(kThreadsK, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(C::KB_SFULL + i), 1);
       mbar_init(bar(C::KB_DPFULL + i), 1);
-      mbar_init(bar(C::KB_PFULL + i), 16);  // one arrive per compute warp
+      mbar_init(bar(C::KB_PFULL + i), 8);  // one arrive per compute warp
     }
     mbar_init(bar(C::KB_ACC), 1);
     mbar_init(bar(C::KB_DONE), 2);  // both MMA issuers
@@ -391,18 +393,18 @@ __global__ void __launch_bounds__(kThreadsK, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp < 16) {
+  if (warp < 8) {
     // ========================================================= P^T and dS^T
     // A unit (q-head, 128-query tile) is processed as two halves of 64
     // queries; half v uses TMEM buffer v & 1 (S^T at 256 + 128 (v & 1), dP^T
     // 64 columns further), so the tensor core computes the next half's S^T
     // and dP^T while the threads turn this half's into P^T and dS^T.
-    const int qd = warp & 3, cq = warp >> 2;  // TMEM lane quarter, query-column quarter
+    const int qd = warp & 3, cq = warp >> 2;  // TMEM lane quarter, query-column half
     const int t = qd * 32 + lane;  // key row of the tile = TMEM lane
     const uint32_t lanes = tmem + ((uint32_t)(qd * 32) << 16);
     const int64_t j = j0 + t;
     const float sl2 = p.scale_log2;
-    const int c0 = 16 * cq;  // query columns [c0, c0 + 16) of every half
+    const int c0 = 32 * cq;  // query columns [c0, c0 + 32) of every half
     bool ok = true;
     for (int v = 0; v < 2 * NU; ++v) {
       const int u = v >> 1, hh = v & 1, bf = v & 1;
@@ -422,12 +424,12 @@ __global__ void __launch_bounds__(kThreadsK, 1)
       const uint32_t sbuf = lanes + 256u + 128u * (uint32_t)bf;
       // P^T from S^T first: the exponentials overlap the dP^T product, which
       // is only waited for before dS^T
-      uint32_t sr[16], dr[16];
-      tmem_ld16(sbuf + (uint32_t)c0, sr);
+      uint32_t sr[32], dr[32];
+      tmem_ld32(sbuf + (uint32_t)c0, sr);
       {
-        uint32_t pp[8];
+        uint32_t pp[2][8];
 #pragma unroll
-        for (int e4 = 0; e4 < 4; ++e4) {
+        for (int e4 = 0; e4 < 8; ++e4) {
           const float4 l4 = lse4[(q0 >> 2) + e4];
           const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
@@ -441,23 +443,25 @@ __global__ void __launch_bounds__(kThreadsK, 1)
               if (c0 + e < lim) p0 = 0.f;
               if (c0 + e + 1 < lim) p1 = 0.f;
             }
-            pp[e >> 1] = Pack16<TIn>::pack2(p0, p1);
+            pp[e >> 4][(e >> 1) & 7] = Pack16<TIn>::pack2(p0, p1);
             sr[e] = __float_as_uint(p0);
             sr[e + 1] = __float_as_uint(p1);
           }
         }
-        // P^T packed over the first 8 of the S^T columns this warp has read
-        tmem_st8(sbuf + (uint32_t)c0, pp);
+        // P^T of query blocks 2 cq and 2 cq + 1, each packed over the first
+        // 8 of its 16 columns
+        tmem_st8(sbuf + (uint32_t)c0, pp[0]);
+        tmem_st8(sbuf + (uint32_t)c0 + 16u, pp[1]);
       }
       if (!__all_sync(0xffffffffu, wait_bar(bar(C::KB_DPFULL + bf), (uint32_t)((v >> 1) & 1), ctl))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      tmem_ld16(sbuf + 64u + (uint32_t)c0, dr);
-      uint32_t pd[8];
+      tmem_ld32(sbuf + 64u + (uint32_t)c0, dr);
+      uint32_t pd[2][8];
 #pragma unroll
-      for (int e4 = 0; e4 < 4; ++e4) {
+      for (int e4 = 0; e4 < 8; ++e4) {
         const float4 d4 = dsm4[(q0 >> 2) + e4];
         const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
@@ -467,18 +471,18 @@ __global__ void __launch_bounds__(kThreadsK, 1)
               make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
               __fadd2_rn(make_float2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])),
                          make_float2(-dv[k], -dv[k + 1])));
-          pd[e >> 1] = f16x2(ds.x, ds.y);
+          pd[e >> 4][(e >> 1) & 7] = f16x2(ds.x, ds.y);
         }
       }
-      // dS^T packed over the first 8 of the dP^T columns this warp has read
-      tmem_st8(sbuf + 64u + (uint32_t)c0, pd);
+      tmem_st8(sbuf + 64u + (uint32_t)c0, pd[0]);
+      tmem_st8(sbuf + 64u + (uint32_t)c0 + 16u, pd[1]);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(C::KB_PFULL + bf));
     }
     // ---- epilogue: dV straight from TMEM; dK = R(j)^T (scale dK~) through a
-    // padded fp32 row per key (the rotation pairs dims across the quarters).
+    // padded fp32 row per key (the rotation pairs dims across the two halves).
     // A non-finite accumulator value (a dS^T term past the fp16 range reaches
     // every dK~ dim of its key) records RA_ERR_RANGE.
     const bool acc = ok && NU > 0 &&
@@ -489,7 +493,7 @@ __global__ void __launch_bounds__(kThreadsK, 1)
     TIn *dvd = static_cast<TIn *>(p.dv) + b * p.sdv0 + hk * p.sdv1 + j * p.sdv2;
     TIn *dkd = static_cast<TIn *>(p.dk) + b * p.sdk0 + hk * p.sdk1 + j * p.sdk2;
     const bool row_ok = j < p.Sk;
-    constexpr int QD = D / 4;  // dims per column quarter
+    constexpr int QD = D / 2;  // dims per column half
     uint32_t bad = 0;
 #pragma unroll 1
     for (int c = 0; c < QD / 16; ++c) {
@@ -518,8 +522,8 @@ __global__ void __launch_bounds__(kThreadsK, 1)
       for (int e = 0; e < 16; ++e) row[col + e] = acc ? __uint_as_float(r[e]) * p.scale : 0.f;
     }
     record_range_flag(p.status, bad);
-    named_bar_sync(1, 512);  // all quarters of every row are in shared memory
-    if (write && row_ok) store_row<D, TIn>(row, true, j, dkd, cq * (D / 32), (cq + 1) * (D / 32), p);
+    named_bar_sync(1, 256);  // both halves of every row are in shared memory
+    if (write && row_ok) store_row<D, TIn>(row, true, j, dkd, cq * (D / 16), (cq + 1) * (D / 16), p);
   } else if (warp == kWarpTmaK) {
     // ============================================= TMA and row statistics
     if (lane == 0) {
