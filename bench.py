@@ -64,6 +64,8 @@ DEC = wl.DECODE_ATTN
 ATTN_KERNEL_SRC = os.path.join(ROOT, "rope_causal_attention_gb300", "csrc", "attn_tc.cu")
 ROPE_KERNEL_SRC = os.path.join(ROOT, "rope_causal_attention_gb300", "csrc", "rope_kernels.cu")
 DECODE_KERNEL_SRC = os.path.join(ROOT, "rope_causal_attention_gb300", "csrc", "decode_tc.cu")
+BWD_KERNEL_SRC = [os.path.join(ROOT, "rope_causal_attention_gb300", "csrc", f)
+                  for f in ("attn_bwd_tc.cu", "attn_bwd_simt.cu")]
 PROFILE_JSON = os.path.join(ROOT, "profiles", "counters.json")
 
 
@@ -95,9 +97,14 @@ def max_over_ranks(value: float) -> float:
     return float(t.item())
 
 
-def src_hash(path):
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def src_hash(paths):
+    """First 16 hex digits of the SHA-256 of one source file, or of several
+    concatenated in order."""
+    h = hashlib.sha256()
+    for path in [paths] if isinstance(paths, str) else paths:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def dram_traffic(kernel_key, src):
@@ -802,7 +809,9 @@ def run_ours(args, ws, rank, local):
                      "kernels": bw["kernels"],
                      "roofline": {"bound": "tensor", "achieved": bw["tflops"], "peak": tf_peak,
                                   "unit": "TFLOP/s", "frac": bw["tflops"] / tf_peak,
-                                  "traffic": None,
+                                  "traffic": dram_traffic("attn_bwd_long_gqa", BWD_KERNEL_SRC),
+                                  "traffic_scope": "DRAM bytes of one whole backward call "
+                                                   "(row term, Q and K rotation, dK/dV, dQ)",
                                   "peak_kind": f"{peak_kind} bf16 dense (burst)",
                                   "note": "2.5x the forward's FLOPs (S, dP, dV, dK, dQ); the "
                                           "kernels recompute S and dP once more for dQ"},
