@@ -41,8 +41,8 @@ def _cases(seed, n, max_work, max_sq):
     return out
 
 
-FWD = _cases(2026, 24, 4e10, 1600)
-BWD = _cases(2027, 8, 2e9, 600)
+FWD = _cases(2026, 48, 4e10, 1600)
+BWD = _cases(2027, 16, 2e9, 600)
 
 
 def _id(c):
